@@ -1,0 +1,154 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4_gb300.so: NVFP4 block quantization of bf16
+ * weight tensors on an sm_103 GPU (GB300).
+ *
+ * NVFP4 here means: 4-bit E2M1 codes, one FP8 E4M3 scale Delta_i per block of
+ * 16 consecutive elements of a row, and one fp32 tensor scale alpha, so that an
+ * element dequantizes to q * alpha * Delta_i.  Sources of the method:
+ *   [SOAR]  "SOAR: Scale Optimization for Accurate Reconstruction in NVFP4
+ *           Quantization" (july-h5kf3.github.io notes): the NVFP4 quantizer
+ *           equation (alpha = max|W| / (6*448), Delta_i = e4m3(max|W_i| /
+ *           (6 alpha)), piecewise FP4 rounding), the dequantization equation,
+ *           CJSO (closed forms for alpha* and Delta_i*, schedule) and the
+ *           decoupled quantization / dequantization scale search.
+ *   [FOS]   "SOAR 周冠军笔记 07 | 香草小张：NVFP4 量化改进与推测解码实践"
+ *           (openbmb.cn blog), section 01 (E2M1 value set) and section 02
+ *           (FourOverSix: scale_m4 = fp8(scale_m6 * 1.5), keep the lower MSE).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or keeps them.  Every call is asynchronous on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream); outputs are valid
+ *     once the stream has reached the call's end.
+ *   - W is bf16, row-major [rows, cols], contiguous.  cols must be a multiple
+ *     of 16 (one block = 16 consecutive elements of a row).
+ *   - codes: rows*cols/2 bytes, row-major [rows, cols/2]; byte k of a row holds
+ *     element 2k in its low nibble and element 2k+1 in its high nibble; bit 3
+ *     of a nibble is the sign, bits 0-2 index {0,0.5,1,1.5,2,3,4,6}.
+ *   - scales: rows*cols/16 bytes, row-major [rows, cols/16], E4M3FN bit
+ *     patterns (linear layout, not swizzled).
+ *   - alpha: one fp32 on the device.
+ *   - Arguments are checked on the host before anything is enqueued; on an
+ *     error nothing is enqueued and a nonzero status is returned.
+ *   - Inputs must be finite, and either all zero or with max|W| >= 2^-64; for
+ *     other inputs the outputs are unspecified (no memory is touched beyond
+ *     the documented buffers either way).
+ *   - Calls on different streams may run concurrently; the library keeps no
+ *     per-call global state.  Scratch memory comes from a library-owned,
+ *     stream-ordered memory pool (cudaMallocFromPoolAsync / cudaFreeAsync on
+ *     `stream`); it is a few tens of KB per call.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, negative size, cols % 16 != 0, bad mode/iters, size overflow */
+  NVFP4_ERR_MISALIGNED = 2,         /* W/out not 16-byte aligned, codes or alpha not 4-byte aligned */
+  NVFP4_ERR_CUDA = 3,               /* a CUDA runtime call or launch failed */
+  NVFP4_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+  NVFP4_ERR_OUT_OF_MEMORY = 5       /* the scratch allocation failed */
+};
+
+/* Scale rules ([SOAR] quantizer equation; [FOS] section 02; [SOAR] CJSO and
+ * decoupled search). */
+enum nvfp4_mode {
+  NVFP4_MODE_MAX = 0,            /* Delta_i = e4m3(amax_i / (6 alpha)) */
+  NVFP4_MODE_FOUR_OVER_SIX = 1,  /* per block: the max-rule scale, or e4m3(1.5 * it) if that
+                                    gives a strictly lower dequantization error */
+  NVFP4_MODE_CJSO = 2,           /* max rule, then `iters` rounds of: alpha* (closed form),
+                                    re-quantize, Delta_i* (closed form, rounded to E4M3),
+                                    re-quantize */
+  NVFP4_MODE_CJSO_DECOUPLED = 3  /* CJSO(iters), then per block a search over 101 quantization
+                                    scales Delta^d0 * {0.50, 0.51, ..., 1.50} and, for each, the
+                                    two E4M3 values bracketing it as the stored scale; the pair
+                                    with the least reconstruction error is kept */
+};
+
+/*
+ * nvfp4_quantize -- bf16 W [rows, cols] -> codes, scales, alpha.
+ *   [SOAR] quantizer equation (alpha, Delta_i, FP4 rounding); mode-specific
+ *   passages as listed for enum nvfp4_mode.
+ * Arguments:
+ *   W      device, bf16, 16-byte aligned; rows*cols elements.
+ *   rows   >= 0.  cols >= 0, cols % 16 == 0.  rows*cols < 2^40.
+ *   mode   an nvfp4_mode value.
+ *   iters  CJSO iterations, 0..64 (modes 2 and 3); ignored by modes 0 and 1.
+ *   codes  device, 4-byte aligned, rows*cols/2 bytes (written).
+ *   scales device, rows*cols/16 bytes (written).
+ *   alpha  device, 4-byte aligned, 1 float (written; 0 for an empty or all-zero W).
+ *   stream cudaStream_t.
+ * Returns an nvfp4_status.  rows*cols == 0 is valid: only *alpha = 0 is written
+ * (W, codes and scales may then be NULL).
+ */
+int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iters,
+                   uint8_t *codes, uint8_t *scales, float *alpha, cudaStream_t stream);
+
+/*
+ * nvfp4_dequantize -- codes, scales, alpha -> bf16 out [rows, cols],
+ *   out = bf16_rne(q * fl(alpha * Delta_i)).  [SOAR] dequantization equation;
+ *   one path for every scale rule ([FOS] section 02: no kernel change).
+ * Arguments: codes (device, 4-byte aligned, rows*cols/2 bytes), scales (device,
+ *   rows*cols/16 bytes), alpha (device, 1 float), rows/cols as for
+ *   nvfp4_quantize, out (device, bf16, 16-byte aligned, rows*cols elements,
+ *   written), stream.
+ * Returns an nvfp4_status.
+ */
+int nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *alpha,
+                     int64_t rows, int64_t cols, void *out, cudaStream_t stream);
+
+/*
+ * nvfp4_encode_e2m1 -- element-wise fp32 -> E2M1 code (one code per output
+ *   byte, sign in bit 3), rounding to nearest with ties to the even code and
+ *   saturation at 6, exactly as the quantizer rounds x / (alpha * Delta).
+ *   [FOS] section 01 value set; [SOAR] piecewise FP4 rounding.
+ * Arguments: v (device, n floats), n >= 0, out (device, n bytes), stream.
+ */
+int nvfp4_encode_e2m1(const float *v, int64_t n, uint8_t *out, cudaStream_t stream);
+
+/*
+ * nvfp4_encode_e4m3 -- element-wise fp32 (>= 0) -> E4M3FN code, round to
+ *   nearest even, saturating at 448, exactly as the quantizer rounds block
+ *   scales.  [SOAR] quantizer equation (Q_E4M3, M_FP8 = 448).
+ * Arguments: v (device, n floats), n >= 0, out (device, n bytes), stream.
+ */
+int nvfp4_encode_e4m3(const float *v, int64_t n, uint8_t *out, cudaStream_t stream);
+
+/*
+ * Kernel tracing.  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on the stream it is launched on, so
+ * per-kernel device time can be read back without an external profiler.
+ * (No counterpart on the method's pages: this is instrumentation.)
+ *   nvfp4_profiler_enable(on)  on != 0 starts recording, 0 stops (recorded
+ *                              launches are kept).  Returns an nvfp4_status.
+ *   nvfp4_profiler_reset()     forgets every record.
+ *   nvfp4_profiler_kinds()     waits for the recorded events, folds them into
+ *                              per-kernel totals and returns the number of
+ *                              distinct kernels seen (< 0 on a CUDA error).
+ *   nvfp4_profiler_get(i, name, name_len, launches, total_ms)
+ *                              kernel i (0 <= i < kinds): its name (NUL-
+ *                              terminated, truncated to name_len), launch
+ *                              count and summed device milliseconds.
+ * Host cost: about two cudaEventRecord calls per launch while enabled.
+ */
+int nvfp4_profiler_enable(int on);
+int nvfp4_profiler_reset(void);
+int nvfp4_profiler_kinds(void);
+int nvfp4_profiler_get(int index, char *name, int name_len, int64_t *launches, double *total_ms);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char *nvfp4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,183 @@
+"""GB300-native NVFP4 block quantization: Python binding of libnvfp4_gb300.so.
+
+The functions named like the C ABI (``nvfp4_quantize``, ``nvfp4_dequantize``,
+``nvfp4_encode_e2m1``, ``nvfp4_encode_e4m3``, ``nvfp4_status_string``) take
+raw device pointers and sizes and return the C status code, exactly as
+declared in include/nvfp4.h.  ``quantize`` / ``dequantize`` / ``encode_*``
+are conveniences over them that take torch tensors (torch supplies device
+memory and the current stream; every step of the computation runs in the
+library's CUDA kernels).  There is no fallback: if the library is missing or
+fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH, build as _build
+
+MAX, FOUR_OVER_SIX, CJSO, CJSO_DECOUPLED = 0, 1, 2, 3
+MODES = {"max": MAX, "four_over_six": FOUR_OVER_SIX, "cjso": CJSO, "cjso_decoupled": CJSO_DECOUPLED}
+
+NVFP4_OK = 0
+
+_lib = None
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({nvfp4_status_string(status)})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads the CUDA library (building it first if it is absent or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = _build()
+    if not os.path.exists(path):
+        raise ImportError(f"NVFP4 CUDA library not found at {path}")
+    L = ctypes.CDLL(path)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.nvfp4_quantize.argtypes = [vp, i64, i64, ci, ci, vp, vp, vp, vp]
+    L.nvfp4_quantize.restype = ci
+    L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    L.nvfp4_dequantize.restype = ci
+    L.nvfp4_encode_e2m1.argtypes = [vp, i64, vp, vp]
+    L.nvfp4_encode_e2m1.restype = ci
+    L.nvfp4_encode_e4m3.argtypes = [vp, i64, vp, vp]
+    L.nvfp4_encode_e4m3.restype = ci
+    L.nvfp4_profiler_enable.argtypes = [ci]
+    L.nvfp4_profiler_enable.restype = ci
+    L.nvfp4_profiler_reset.argtypes = []
+    L.nvfp4_profiler_reset.restype = ci
+    L.nvfp4_profiler_kinds.argtypes = []
+    L.nvfp4_profiler_kinds.restype = ci
+    L.nvfp4_profiler_get.argtypes = [ci, ctypes.c_char_p, ci, ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_double)]
+    L.nvfp4_profiler_get.restype = ci
+    L.nvfp4_status_string.argtypes = [ci]
+    L.nvfp4_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+# ---------------------------------------------------------------- C ABI mirror
+
+def nvfp4_quantize(W, rows, cols, mode, iters, codes, scales, alpha, stream) -> int:
+    return load().nvfp4_quantize(W, rows, cols, mode, iters, codes, scales, alpha, stream)
+
+
+def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
+    return load().nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream)
+
+
+def nvfp4_encode_e2m1(v, n, out, stream) -> int:
+    return load().nvfp4_encode_e2m1(v, n, out, stream)
+
+
+def nvfp4_encode_e4m3(v, n, out, stream) -> int:
+    return load().nvfp4_encode_e4m3(v, n, out, stream)
+
+
+def nvfp4_status_string(status: int) -> str:
+    return load().nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_profiler_enable(on: int) -> int:
+    return load().nvfp4_profiler_enable(int(on))
+
+
+def nvfp4_profiler_reset() -> int:
+    return load().nvfp4_profiler_reset()
+
+
+def nvfp4_profiler_kinds() -> int:
+    return load().nvfp4_profiler_kinds()
+
+
+def nvfp4_profiler_get(index, name, name_len, launches, total_ms) -> int:
+    return load().nvfp4_profiler_get(index, name, name_len, launches, total_ms)
+
+
+def profiler_report() -> dict:
+    """{kernel name: (launches, total device ms)} of the traced launches."""
+    n = nvfp4_profiler_kinds()
+    if n < 0:
+        raise Nvfp4Error(-n, "nvfp4_profiler_kinds")
+    out = {}
+    for i in range(n):
+        buf = ctypes.create_string_buffer(64)
+        cnt = ctypes.c_int64()
+        ms = ctypes.c_double()
+        _check(nvfp4_profiler_get(i, buf, 64, ctypes.byref(cnt), ctypes.byref(ms)), "nvfp4_profiler_get")
+        out[buf.value.decode()] = (int(cnt.value), float(ms.value))
+    return out
+
+
+# ------------------------------------------------------------ torch helpers
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != NVFP4_OK:
+        raise Nvfp4Error(status, what)
+
+
+def quantize(W, mode=MAX, iters: int = 0, out=None, stream=None):
+    """Quantizes a contiguous bf16 CUDA tensor [rows, cols] (cols % 16 == 0).
+
+    Returns (codes uint8 [rows, cols/2], scales uint8 [rows, cols/16] holding
+    E4M3 bit patterns, alpha float32 [1]), all on W's device.  `out` may pass
+    preallocated (codes, scales, alpha) tensors."""
+    import torch
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    if W.dtype != torch.bfloat16 or not W.is_cuda or W.dim() != 2 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous 2-D bf16 CUDA tensor")
+    rows, cols = W.shape
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=W.device)
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=W.device)
+        alpha = torch.empty(1, dtype=torch.float32, device=W.device)
+    else:
+        codes, scales, alpha = out
+    st = nvfp4_quantize(W.data_ptr(), rows, cols, int(mode), int(iters), codes.data_ptr(), scales.data_ptr(),
+                        alpha.data_ptr(), _stream_ptr(stream))
+    _check(st, "nvfp4_quantize")
+    return codes, scales, alpha
+
+
+def dequantize(codes, scales, alpha, rows: int, cols: int, out=None, stream=None):
+    """Returns the bf16 CUDA tensor [rows, cols] that the NVFP4 tensor encodes."""
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=codes.device)
+    st = nvfp4_dequantize(codes.data_ptr(), scales.data_ptr(), alpha.data_ptr(), rows, cols, out.data_ptr(),
+                          _stream_ptr(stream))
+    _check(st, "nvfp4_dequantize")
+    return out
+
+
+def encode_e2m1(v, stream=None):
+    import torch
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(nvfp4_encode_e2m1(v.data_ptr(), v.numel(), out.data_ptr(), _stream_ptr(stream)), "nvfp4_encode_e2m1")
+    return out
+
+
+def encode_e4m3(v, stream=None):
+    import torch
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(nvfp4_encode_e4m3(v.data_ptr(), v.numel(), out.data_ptr(), _stream_ptr(stream)), "nvfp4_encode_e4m3")
+    return out

@@ -1,0 +1,333 @@
+// nvfp4_api.cu -- the C ABI declared in include/nvfp4.h: argument checks,
+// scratch allocation from a stream-ordered pool, and the launch sequence of
+// each scale rule.
+//
+// Launch sequences (all on the caller's stream):
+//   max / FourOverSix : amax partials -> quantize (folds the partials itself)
+//   CJSO(T)           : amax partials -> init sweep -> T iteration sweeps
+//                       (each folds the previous sweep's partial sums)
+//   decoupled CJSO(T) : the CJSO(T) sweeps without codes -> decoupled search
+//   dequantize        : one kernel
+// Grid-wide dependencies are kernel boundaries: no kernel waits on another
+// CTA, so nothing can spin.
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/nvfp4.h"
+#include "nvfp4_internal.h"
+
+namespace {
+
+using namespace nvfp4;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxIters = 64;
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+struct DevInfo {
+  bool ready = false;
+  int status = NVFP4_OK;
+  int sms = 0;
+  int occ[6] = {1, 1, 1, 1, 1, 1};
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+int map_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return NVFP4_OK;
+  if (e == cudaErrorMemoryAllocation) return NVFP4_ERR_OUT_OF_MEMORY;
+  return NVFP4_ERR_CUDA;
+}
+
+// Per-device facts, queried once: SM count, occupancy of every kernel and a
+// library-owned memory pool that keeps its memory (release threshold = max),
+// so steady-state scratch allocations never reach the driver.
+int device_info(DevInfo **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return map_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return map_cuda(e);
+    if (major != 10 || minor != 3) {
+      d.status = NVFP4_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      for (int k = 0; k < 6; ++k) d.occ[k] = max_active_ctas(k);
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&d.pool, &props);
+      if (e != cudaSuccess) return map_cuda(e);
+      uint64_t keep = UINT64_MAX;
+      e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e != cudaSuccess) return map_cuda(e);
+      d.status = NVFP4_OK;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.status;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % 16 != 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && cols > kMaxElems / rows) return NVFP4_ERR_INVALID_ARG;
+  if (rows * cols >= kMaxElems) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+int grid_for(const DevInfo &d, int kern, int64_t work_items) {
+  int64_t full = int64_t(d.sms) * d.occ[kern];
+  int64_t need = (work_items + 255) / 256;
+  if (need < 1) need = 1;
+  return (int)(need < full ? need : full);
+}
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Kernel tracing: CUDA events around each launch while enabled.
+// ---------------------------------------------------------------------------
+
+enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
+       kTrKinds };
+const char *const kTraceNames[kTrKinds] = {"k_amax_partials",   "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
+                                           "k_cjso_sweep<init>", "k_cjso_sweep<iter>",   "k_decoupled",
+                                           "k_dequant",          "k_encode"};
+
+struct TraceRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_tr_mu;
+bool g_tr_on = false;
+std::vector<TraceRec> g_tr_pending;
+int64_t g_tr_launches[kTrKinds] = {};
+double g_tr_ms[kTrKinds] = {};
+
+// Records the start event (if tracing) before a launch and the stop event after.
+struct TraceScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  TraceScope(int k, cudaStream_t s) : kind(k), st(s) {
+    bool on;
+    {
+      std::lock_guard<std::mutex> lock(g_tr_mu);
+      on = g_tr_on;
+    }
+    if (!on) return;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess ||
+        cudaEventRecord(a, st) != cudaSuccess) {
+      if (a) cudaEventDestroy(a);
+      if (b) cudaEventDestroy(b);
+      a = b = nullptr;
+    }
+  }
+  ~TraceScope() {
+    if (!a) return;
+    if (cudaEventRecord(b, st) != cudaSuccess) {
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+      return;
+    }
+    std::lock_guard<std::mutex> lock(g_tr_mu);
+    g_tr_pending.push_back({kind, a, b});
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char *nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_MISALIGNED: return "misaligned pointer";
+    case NVFP4_ERR_CUDA: return "CUDA runtime error";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case NVFP4_ERR_OUT_OF_MEMORY: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iters, uint8_t *codes,
+                   uint8_t *scales, float *alpha, cudaStream_t stream) {
+  int st = check_shape(rows, cols);
+  if (st != NVFP4_OK) return st;
+  if (mode < kModeMax || mode > kModeCjsoDecoupled || !alpha) return NVFP4_ERR_INVALID_ARG;
+  const bool cjso = mode == kModeCjso || mode == kModeCjsoDecoupled;
+  if (cjso && (iters < 0 || iters > kMaxIters)) return NVFP4_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!W || !codes || !scales)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(alpha, 4) || (n > 0 && (!aligned(W, 16) || !aligned(codes, 4)))) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (n == 0) return map_cuda(cudaMemsetAsync(alpha, 0, sizeof(float), stream));
+
+  const int64_t H = n / 8;   // half blocks = 16-byte loads
+  const int64_t B = n / 16;  // blocks
+  const int T = cjso ? iters : 0;
+  const int g_amax = grid_for(*d, kKernAmax, H / 4 + 1);
+  const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, H);
+  const int g_cjso = grid_for(*d, kKernCjso, H);
+  const int g_dec = grid_for(*d, kKernDecoupled, B);
+
+  // scratch: amax partials | 2 x CJSO partial sums | alpha history
+  const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);
+  const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 16, 256);
+  const int64_t ws_bytes = off_hist + round_up(int64_t(kMaxIters + 1) * 4, 256);
+  void *ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)ws_bytes, d->pool, stream);
+  if (e != cudaSuccess) return map_cuda(e);
+  char *base = static_cast<char *>(ws);
+  uint32_t *amax_part = reinterpret_cast<uint32_t *>(base);
+  float4 *part[2] = {reinterpret_cast<float4 *>(base + off_part),
+                     reinterpret_cast<float4 *>(base + off_part) + g_cjso};
+  float *hist = reinterpret_cast<float *>(base + off_hist);
+
+  {
+    TraceScope tr(kTrAmax, stream);
+    e = launch_amax_partials(W, H, amax_part, g_amax, stream);
+  }
+  if (e == cudaSuccess && !cjso) {
+    TraceScope tr(mode == kModeFourOverSix ? kTrQuantFos : kTrQuantMax, stream);
+    e = launch_quant_max_fos(mode, W, H, amax_part, g_amax, codes, scales, alpha, g_quant, stream);
+  } else if (e == cudaSuccess) {
+    const bool plain = mode == kModeCjso;
+    {
+      TraceScope tr(kTrCjsoInit, stream);
+      e = launch_cjso_sweep(true, W, H, amax_part, g_amax, nullptr, 0, part[0], hist, 0, scales, codes,
+                            plain && T == 0, alpha, T == 0, g_cjso, stream);
+    }
+    for (int t = 1; t <= T && e == cudaSuccess; ++t) {
+      TraceScope tr(kTrCjsoIter, stream);
+      e = launch_cjso_sweep(false, W, H, amax_part, g_amax, part[(t - 1) & 1], g_cjso, part[t & 1], hist, t,
+                            scales, codes, plain && t == T, alpha, t == T, g_cjso, stream);
+    }
+    if (e == cudaSuccess && !plain) {
+      TraceScope tr(kTrDecoupled, stream);
+      e = launch_decoupled(W, B, hist, T, scales, codes, g_dec, stream);
+    }
+  }
+  // The scratch goes back to the pool in stream order, after the last kernel.
+  cudaError_t ef = cudaFreeAsync(ws, stream);
+  return map_cuda(e != cudaSuccess ? e : ef);
+}
+
+int nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows, int64_t cols,
+                     void *out, cudaStream_t stream) {
+  int st = check_shape(rows, cols);
+  if (st != NVFP4_OK) return st;
+  const int64_t n = rows * cols;
+  if (!alpha || (n > 0 && (!codes || !scales || !out))) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(alpha, 4) || (n > 0 && (!aligned(codes, 4) || !aligned(out, 16)))) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (n == 0) return NVFP4_OK;
+  const int64_t H = n / 8;
+  TraceScope tr(kTrDequant, stream);
+  return map_cuda(launch_dequant(codes, scales, alpha, H, out, grid_for(*d, kKernDequant, H), stream));
+}
+
+int nvfp4_encode_e2m1(const float *v, int64_t n, uint8_t *out, cudaStream_t stream) {
+  if (n < 0 || n >= kMaxElems || (n > 0 && (!v || !out))) return NVFP4_ERR_INVALID_ARG;
+  if (n > 0 && !aligned(v, 4)) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (n == 0) return NVFP4_OK;
+  TraceScope tr(kTrEncode, stream);
+  return map_cuda(launch_encode_e2m1(v, n, out, grid_for(*d, kKernDequant, n), stream));
+}
+
+int nvfp4_encode_e4m3(const float *v, int64_t n, uint8_t *out, cudaStream_t stream) {
+  if (n < 0 || n >= kMaxElems || (n > 0 && (!v || !out))) return NVFP4_ERR_INVALID_ARG;
+  if (n > 0 && !aligned(v, 4)) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (n == 0) return NVFP4_OK;
+  TraceScope tr(kTrEncode, stream);
+  return map_cuda(launch_encode_e4m3(v, n, out, grid_for(*d, kKernDequant, n), stream));
+}
+
+int nvfp4_profiler_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_tr_mu);
+  g_tr_on = on != 0;
+  return NVFP4_OK;
+}
+
+int nvfp4_profiler_reset(void) {
+  std::lock_guard<std::mutex> lock(g_tr_mu);
+  for (auto &r : g_tr_pending) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_tr_pending.clear();
+  for (int k = 0; k < kTrKinds; ++k) {
+    g_tr_launches[k] = 0;
+    g_tr_ms[k] = 0.0;
+  }
+  return NVFP4_OK;
+}
+
+int nvfp4_profiler_kinds(void) {
+  std::lock_guard<std::mutex> lock(g_tr_mu);
+  int status = 0;
+  for (auto &r : g_tr_pending) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e == cudaSuccess) {
+      g_tr_launches[r.kind] += 1;
+      g_tr_ms[r.kind] += ms;
+    } else {
+      status = -NVFP4_ERR_CUDA;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_tr_pending.clear();
+  if (status < 0) return status;
+  int n = 0;
+  for (int k = 0; k < kTrKinds; ++k) n += g_tr_launches[k] > 0;
+  return n;
+}
+
+int nvfp4_profiler_get(int index, char *name, int name_len, int64_t *launches, double *total_ms) {
+  std::lock_guard<std::mutex> lock(g_tr_mu);
+  int seen = -1;
+  for (int k = 0; k < kTrKinds; ++k) {
+    if (g_tr_launches[k] == 0) continue;
+    if (++seen != index) continue;
+    if (name && name_len > 0) {
+      std::strncpy(name, kTraceNames[k], (size_t)name_len - 1);
+      name[name_len - 1] = '\0';
+    }
+    if (launches) *launches = g_tr_launches[k];
+    if (total_ms) *total_ms = g_tr_ms[k];
+    return NVFP4_OK;
+  }
+  return NVFP4_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

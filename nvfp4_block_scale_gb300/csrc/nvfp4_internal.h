@@ -1,0 +1,28 @@
+// nvfp4_internal.h -- launchers shared between the kernels and the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+#include <vector_types.h>
+
+namespace nvfp4 {
+
+enum { kModeMax = 0, kModeFourOverSix = 1, kModeCjso = 2, kModeCjsoDecoupled = 3 };
+enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDecoupled, kKernDequant };
+
+cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
+cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
+                          uint8_t *codes, uint8_t *scales, float *alpha, int grid, cudaStream_t st);
+cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
+                       const float4 *part_in, int n_in, float4 *part_out, float *alpha_hist, int t,
+                       uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
+                       int grid, cudaStream_t st);
+cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,
+                      int grid, cudaStream_t st);
+cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out, int grid,
+                    cudaStream_t st);
+cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
+cudaError_t launch_encode_e4m3(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
+int max_active_ctas(int which);
+
+}  // namespace nvfp4

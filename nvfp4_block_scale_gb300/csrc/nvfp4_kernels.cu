@@ -1,0 +1,480 @@
+// nvfp4_kernels.cu -- sm_103a kernels of the NVFP4 quantization hot path.
+//
+// Work unit: a "half block" = 8 consecutive bf16 = one 16-byte load.  Two
+// adjacent lanes of a warp hold one 16-element block and combine their block
+// amax and sums with one shuffle.  Warps walk the tensor in tiles of 32 half
+// blocks (512 contiguous bytes per warp per load: fully coalesced), grid-stride.
+//
+// Citation keys (page title, part of the page):
+//   [SOAR-Q]   "SOAR: Scale Optimization for Accurate Reconstruction in NVFP4
+//              Quantization": NVFP4 quantizer equation.
+//   [SOAR-DQ]  same page: dequantization equation.
+//   [SOAR-A]   same page: closed form for the global scale alpha*.
+//   [SOAR-D]   same page: closed form for a block scale Delta_i*.
+//   [SOAR-SCHED] same page: CJSO schedule (max-rule start, re-quantize after
+//              every update).
+//   [SOAR-DEC] same page: decoupled quantization/dequantization scale search.
+//   [FOS-02]   "SOAR 周冠军笔记 07 | 香草小张：NVFP4 量化改进与推测解码实践",
+//              section 02 (FourOverSix).
+#include <cuda_runtime.h>
+
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// ---------------------------------------------------------------------------
+// Block-wide reductions
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+  v = __reduce_max_sync(0xFFFFFFFFu, v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = lane < kWarps ? red[lane] : 0u;
+    t = __reduce_max_sync(0xFFFFFFFFu, t);
+    if (lane == 0) red[0] = t;
+  }
+  __syncthreads();
+  uint32_t r = red[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void warp_ff_sum(FF &a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float h = __shfl_xor_sync(0xFFFFFFFFu, a.hi, o);
+    float l = __shfl_xor_sync(0xFFFFFFFFu, a.lo, o);
+    ff_add(a, h, l);
+  }
+}
+
+// Sums two compensated accumulators over the CTA in a fixed order; the
+// result is valid in thread 0.
+__device__ __forceinline__ void block_ff_sum2(FF &a, FF &b, float4 *red) {
+  warp_ff_sum(a);
+  warp_ff_sum(b);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = make_float4(a.hi, a.lo, b.hi, b.lo);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    FF x = {0.0f, 0.0f}, y = {0.0f, 0.0f};
+    for (int w = 0; w < kWarps; ++w) {
+      ff_add(x, red[w].x, red[w].y);
+      ff_add(y, red[w].z, red[w].w);
+    }
+    a = x;
+    b = y;
+  }
+  __syncthreads();
+}
+
+// [SOAR-Q] alpha = max|W| / (6*448), from the per-CTA amax partials.
+__device__ __forceinline__ float fold_alpha(const uint32_t *__restrict__ part, int n, uint32_t *red) {
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) m = max(m, part[i]);
+  m = block_max_u32(m, red);
+  return __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+}
+
+// Per-CTA tables over all 128 non-negative E4M3 codes: dequant scale
+// s = fl(alpha*Delta) and its IEEE reciprocal (0 where s == 0).
+__device__ __forceinline__ void build_scale_tables(float alpha, float *s_tab, float *r_tab) {
+  if (threadIdx.x < 128) {
+    float s = __fmul_rn(alpha, e4m3_value(threadIdx.x));
+    s_tab[threadIdx.x] = s;
+    r_tab[threadIdx.x] = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  }
+}
+
+// [SOAR-Q] max rule for one block: Delta = e4m3(fl(amax_i / fl(6 alpha))).
+__device__ __forceinline__ uint32_t max_rule_code(uint32_t amax_bits, float six_a, float r6) {
+  if (!(six_a > 0.0f)) return 0u;
+  return e4m3_code(div_by_scale(__uint_as_float(amax_bits << 16), six_a, r6));
+}
+
+__device__ __forceinline__ uint4 load_half(const uint4 *__restrict__ W, int64_t h, bool valid) {
+  return valid ? __ldg(W + h) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------------------
+// a1: global amax partials
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restrict__ W, int64_t n16,
+                                                            uint32_t *__restrict__ part) {
+  __shared__ uint32_t red[kWarps];
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 a = __ldg(W + i), b = __ldg(W + i + stride), c = __ldg(W + i + 2 * stride),
+          d = __ldg(W + i + 3 * stride);
+    const uint32_t ws[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
+                             c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      uint32_t t = ws[k] & 0x7FFF7FFFu;
+      m2 = __hmax2(m2, *reinterpret_cast<__nv_bfloat162 *>(&t));
+    }
+  }
+  for (; i < n16; i += stride) {
+    uint4 a = __ldg(W + i);
+    const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t t = ws[k] & 0x7FFF7FFFu;
+      m2 = __hmax2(m2, *reinterpret_cast<__nv_bfloat162 *>(&t));
+    }
+  }
+  uint32_t mb = *reinterpret_cast<uint32_t *>(&m2);
+  uint32_t m = max(mb & 0xFFFFu, mb >> 16);
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) part[blockIdx.x] = m;
+}
+
+// ---------------------------------------------------------------------------
+// a2-a4, a7: max rule and FourOverSix
+// ---------------------------------------------------------------------------
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restrict__ W, int64_t H,
+                                                            const uint32_t *__restrict__ amax_part, int n_amax,
+                                                            uint32_t *__restrict__ codes32,
+                                                            uint8_t *__restrict__ scales,
+                                                            float *__restrict__ alpha_out) {
+  __shared__ uint32_t red[kWarps];
+  __shared__ float s_tab[128], r_tab[128];
+  __shared__ uint8_t c4_tab[128];
+  const float alpha = fold_alpha(amax_part, n_amax, red);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *alpha_out = alpha;
+  const float six_a = __fmul_rn(alpha, 6.0f);
+  const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
+  build_scale_tables(alpha, s_tab, r_tab);
+  if (MODE == kModeFourOverSix && threadIdx.x < 128)  // [FOS-02] scale_m4 = fp8(scale_m6 * 1.5)
+    c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(e4m3_value(threadIdx.x), 1.5f));
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t base = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 32; base < H;
+       base += nwarps * 32) {
+    const int64_t h = base + lane;
+    const bool valid = h < H;
+    float ax[8];
+    uint32_t sgn, am;
+    unpack8(load_half(W, h, valid), ax, sgn, am);
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    const uint32_t d6 = max_rule_code(am, six_a, r6);
+    uint32_t d = d6, mags;
+    HalfQ q6 = quant_half(ax, s_tab[d6], r_tab[d6]);
+    if (MODE == kModeFourOverSix) {
+      // [FOS-02] keep scale_m4 iff its dequant error is strictly lower.
+      const uint32_t d4 = c4_tab[d6];
+      HalfQ q4 = quant_half(ax, s_tab[d4], r_tab[d4]);
+      const float P6 = __fadd_rn(q6.P, __shfl_xor_sync(0xFFFFFFFFu, q6.P, 1));
+      const float R6 = __fadd_rn(q6.R, __shfl_xor_sync(0xFFFFFFFFu, q6.R, 1));
+      const float P4 = __fadd_rn(q4.P, __shfl_xor_sync(0xFFFFFFFFu, q4.P, 1));
+      const float R4 = __fadd_rn(q4.R, __shfl_xor_sync(0xFFFFFFFFu, q4.R, 1));
+      const bool use4 = cand_err(s_tab[d4], P4, R4) < cand_err(s_tab[d6], P6, R6);
+      d = use4 ? d4 : d6;
+      mags = use4 ? q4.mags : q6.mags;
+    } else {
+      mags = q6.mags;
+    }
+    if (valid) {
+      codes32[h] = mags | sgn;
+      if (!(lane & 1)) scales[h >> 1] = (uint8_t)d;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a5: CJSO sweeps
+// ---------------------------------------------------------------------------
+
+// One sweep.  INIT: max rule from the amax partials.  Otherwise: alpha from
+// the previous sweep's partial sums ([SOAR-A]), re-quantize with the stored
+// Delta, Delta* ([SOAR-D]) rounded to E4M3, re-quantize ([SOAR-SCHED]).
+// Every sweep stores Delta, writes the partial sums sum Delta*P and
+// sum Delta^2*R of its CTA, and records alpha in alpha_hist[t].
+template <bool INIT>
+__global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict__ W, int64_t H,
+                                                         const uint32_t *__restrict__ amax_part, int n_amax,
+                                                         const float4 *__restrict__ part_in, int n_in,
+                                                         float4 *__restrict__ part_out,
+                                                         float *__restrict__ alpha_hist, int t,
+                                                         uint8_t *__restrict__ scales,
+                                                         uint32_t *__restrict__ codes32, int write_codes,
+                                                         float *__restrict__ alpha_out, int write_alpha) {
+  __shared__ uint32_t red[kWarps];
+  __shared__ float4 redf[kWarps];
+  __shared__ float s_tab[128], r_tab[128];
+  __shared__ float sh_alpha;
+  float alpha;
+  if (INIT) {
+    alpha = fold_alpha(amax_part, n_amax, red);
+  } else {
+    FF num = {0.0f, 0.0f}, den = {0.0f, 0.0f};
+    for (int i = threadIdx.x; i < n_in; i += kThreads) {
+      float4 p = part_in[i];
+      ff_add(num, p.x, p.y);
+      ff_add(den, p.z, p.w);
+    }
+    block_ff_sum2(num, den, redf);
+    if (threadIdx.x == 0) {
+      const double dn = (double)num.hi + (double)num.lo;
+      const double dd = (double)den.hi + (double)den.lo;
+      sh_alpha = dd > 0.0 ? __double2float_rn(__ddiv_rn(dn, dd)) : alpha_hist[t - 1];
+    }
+    __syncthreads();
+    alpha = sh_alpha;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    alpha_hist[t] = alpha;
+    if (write_alpha) *alpha_out = alpha;
+  }
+  const float six_a = __fmul_rn(alpha, 6.0f);
+  const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
+  build_scale_tables(alpha, s_tab, r_tab);
+  __syncthreads();
+
+  FF num = {0.0f, 0.0f}, den = {0.0f, 0.0f};
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t base = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 32; base < H;
+       base += nwarps * 32) {
+    const int64_t h = base + lane;
+    const bool valid = h < H;
+    float ax[8];
+    uint32_t sgn, am;
+    unpack8(load_half(W, h, valid), ax, sgn, am);
+    uint32_t d;
+    HalfQ q;
+    float P, R;
+    if (INIT) {
+      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      d = max_rule_code(am, six_a, r6);
+      q = quant_half(ax, s_tab[d], r_tab[d]);
+    } else {
+      d = valid ? scales[h >> 1] : 0u;
+      q = quant_half(ax, s_tab[d], r_tab[d]);
+      P = __fadd_rn(q.P, __shfl_xor_sync(0xFFFFFFFFu, q.P, 1));
+      R = __fadd_rn(q.R, __shfl_xor_sync(0xFFFFFFFFu, q.R, 1));
+      if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
+      q = quant_half(ax, s_tab[d], r_tab[d]);
+    }
+    P = __fadd_rn(q.P, __shfl_xor_sync(0xFFFFFFFFu, q.P, 1));
+    R = __fadd_rn(q.R, __shfl_xor_sync(0xFFFFFFFFu, q.R, 1));
+    if (valid) {
+      if (write_codes) codes32[h] = q.mags | sgn;
+      if (!(lane & 1)) {
+        scales[h >> 1] = (uint8_t)d;
+        const float dv = e4m3_value(d);
+        ff_add_prod(num, dv, P);                    // exact product, compensated sum
+        ff_add(den, __fmul_rn(__fmul_rn(dv, dv), R), 0.0f);  // Delta^2 * R is exact in fp32
+      }
+    }
+  }
+  block_ff_sum2(num, den, redf);
+  if (threadIdx.x == 0) part_out[blockIdx.x] = make_float4(num.hi, num.lo, den.hi, den.lo);
+}
+
+// ---------------------------------------------------------------------------
+// a6: decoupled search (one thread per block, block held in registers)
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) k_decoupled(const uint4 *__restrict__ W, int64_t B,
+                                                        const float *__restrict__ alpha_hist, int t,
+                                                        uint8_t *__restrict__ scales,
+                                                        uint32_t *__restrict__ codes32) {
+  __shared__ float ev_tab[128], sd_tab[128], m_tab[101];
+  const float alpha = alpha_hist[t];
+  if (threadIdx.x < 128) {
+    const float ev = e4m3_value(threadIdx.x);
+    ev_tab[threadIdx.x] = ev;
+    sd_tab[threadIdx.x] = __fmul_rn(alpha, ev);
+  }
+  if (threadIdx.x < 101)  // [SOAR-DEC] multipliers 0.50, 0.51, ..., 1.50 rounded to fp32
+    m_tab[threadIdx.x] = __double2float_rn(__ddiv_rn((double)(50 + threadIdx.x), 100.0));
+  __syncthreads();
+
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < B; b += (int64_t)gridDim.x * kThreads) {
+    float ax0[8], ax1[8];
+    uint32_t sg0, sg1, am;
+    unpack8(__ldg(W + 2 * b), ax0, sg0, am);
+    unpack8(__ldg(W + 2 * b + 1), ax1, sg1, am);
+    const uint32_t d0 = scales[b];
+    const float delta0 = ev_tab[d0];
+    uint32_t best_d = d0, best_k = 0;
+    bool any = __fmul_rn(alpha, delta0) != 0.0f;
+    if (any) {
+      float best_g = __int_as_float(0x7F800000);  // +inf
+      for (int k = 0; k <= 100; ++k) {
+        const float dq = __fmul_rn(delta0, m_tab[k]);
+        const float sq = __fmul_rn(alpha, dq);
+        const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
+        HalfQ a = quant_half(ax0, sq, rq);
+        HalfQ c = quant_half(ax1, sq, rq);
+        const float P = __fadd_rn(a.P, c.P), R = __fadd_rn(a.R, c.R);
+        // the two E4M3 values bracketing dq (448 above 448)
+        const uint32_t n = e4m3_code(dq);
+        const float vn = ev_tab[n];
+        const uint32_t lo = vn > dq ? n - 1u : n;
+        const uint32_t hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
+        const float glo = cand_err(sd_tab[lo], P, R);
+        const float ghi = cand_err(sd_tab[hi], P, R);
+        if (glo < best_g) { best_g = glo; best_d = lo; best_k = k; }
+        if (ghi < best_g) { best_g = ghi; best_d = hi; best_k = k; }
+      }
+    }
+    uint32_t m0 = 0, m1 = 0;
+    if (any) {
+      const float dq = __fmul_rn(delta0, m_tab[best_k]);
+      const float sq = __fmul_rn(alpha, dq);
+      const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
+      m0 = quant_half(ax0, sq, rq).mags;
+      m1 = quant_half(ax1, sq, rq).mags;
+    }
+    codes32[2 * b] = m0 | sg0;  // two 4-byte stores: codes is only 4-byte aligned
+    codes32[2 * b + 1] = m1 | sg1;
+    scales[b] = (uint8_t)best_d;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a8: dequantize
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) k_dequant(const uint32_t *__restrict__ codes32,
+                                                      const uint8_t *__restrict__ scales,
+                                                      const float *__restrict__ alpha_p, int64_t H,
+                                                      uint4 *__restrict__ out) {
+  __shared__ float s_tab[256];
+  const float alpha = *alpha_p;
+  s_tab[threadIdx.x] = __fmul_rn(alpha, e4m3_value(threadIdx.x));  // kThreads == 256
+  __syncthreads();
+  for (int64_t h = (int64_t)blockIdx.x * kThreads + threadIdx.x; h < H; h += (int64_t)gridDim.x * kThreads) {
+    const uint32_t cw = __ldg(codes32 + h);
+    const float s = s_tab[__ldg(scales + (h >> 1))];
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 q = e2m1x2_to_f32x2((cw >> (8 * k)) & 0xFFu);  // signed codes
+      __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(q.x, s), __fmul_rn(q.y, s));
+      o[k] = *reinterpret_cast<uint32_t *>(&p);
+    }
+    out[h] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// element-wise format conversions (the quantizer's own rounding)
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) k_encode_e2m1(const float *__restrict__ v, int64_t n,
+                                                          uint8_t *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
+    const float x = v[i];
+    const uint32_t mag = cvt_e2m1x2(0.0f, fabsf(x)) & 7u;
+    out[i] = (uint8_t)(mag | ((__float_as_uint(x) >> 31) << 3));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_encode_e4m3(const float *__restrict__ v, int64_t n,
+                                                          uint8_t *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads)
+    out[i] = (uint8_t)e4m3_code(v[i]);
+}
+
+// ---------------------------------------------------------------------------
+// launchers (each returns the launch's own status)
+// ---------------------------------------------------------------------------
+
+namespace {
+cudaLaunchConfig_t make_cfg(int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cfg;
+}
+}  // namespace
+
+cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  return cudaLaunchKernelEx(&cfg, k_amax_partials, static_cast<const uint4 *>(W), n16, part);
+}
+
+cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
+                                 uint8_t *codes, uint8_t *scales, float *alpha, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  const uint4 *w = static_cast<const uint4 *>(W);
+  uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  if (mode == kModeFourOverSix)
+    return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeFourOverSix>, w, H, amax_part, n_amax, c, scales, alpha);
+  return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, H, amax_part, n_amax, c, scales, alpha);
+}
+
+cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
+                              const float4 *part_in, int n_in, float4 *part_out, float *alpha_hist, int t,
+                              uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
+                              int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  const uint4 *w = static_cast<const uint4 *>(W);
+  uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  if (init)
+    return cudaLaunchKernelEx(&cfg, k_cjso_sweep<true>, w, H, amax_part, n_amax, part_in, n_in, part_out,
+                              alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha);
+  return cudaLaunchKernelEx(&cfg, k_cjso_sweep<false>, w, H, amax_part, n_amax, part_in, n_in, part_out,
+                            alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha);
+}
+
+cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
+                             uint8_t *codes, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  return cudaLaunchKernelEx(&cfg, k_decoupled, static_cast<const uint4 *>(W), B, alpha_hist, t, scales,
+                            reinterpret_cast<uint32_t *>(codes));
+}
+
+cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out,
+                           int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  return cudaLaunchKernelEx(&cfg, k_dequant, reinterpret_cast<const uint32_t *>(codes), scales, alpha, H,
+                            static_cast<uint4 *>(out));
+}
+
+cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  return cudaLaunchKernelEx(&cfg, k_encode_e2m1, v, n, out);
+}
+
+cudaError_t launch_encode_e4m3(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  return cudaLaunchKernelEx(&cfg, k_encode_e4m3, v, n, out);
+}
+
+int max_active_ctas(int which) {
+  int n = 0;
+  cudaError_t e = cudaSuccess;
+  switch (which) {
+    case kKernAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
+    case kKernQuantMax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeMax>, kThreads, 0); break;
+    case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
+    case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
+    case kKernDecoupled: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kThreads, 0); break;
+    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_dequant, kThreads, 0); break;
+  }
+  return (e == cudaSuccess && n > 0) ? n : 1;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,77 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+function include/nvfp4.h declares, and rejects bad arguments with the
+documented status before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_block_scale_gb300 as nv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+OK, INVALID, MISALIGNED = 0, 1, 2
+A16 = 0x10000  # fake, suitably aligned device addresses: never dereferenced on these paths
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function():
+    lib = nv.load()
+    names = declared_functions()
+    assert "nvfp4_quantize" in names and "nvfp4_dequantize" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    assert nv.nvfp4_status_string(0) == "ok"
+    for s in range(1, 6):
+        assert nv.nvfp4_status_string(s) not in ("ok", "unknown status")
+    assert nv.nvfp4_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("rows,cols,mode,iters,expect", [
+    (4, 17, 0, 0, INVALID),      # cols % 16 != 0
+    (-1, 16, 0, 0, INVALID),     # negative rows
+    (4, -16, 0, 0, INVALID),
+    (4, 16, 4, 0, INVALID),      # unknown mode
+    (4, 16, -1, 0, INVALID),
+    (4, 16, 2, -1, INVALID),     # CJSO iterations out of range
+    (4, 16, 3, 65, INVALID),
+    (1 << 25, 1 << 16, 0, 0, INVALID),  # 2^41 elements: too large
+])
+def test_quantize_rejects_bad_arguments(rows, cols, mode, iters, expect):
+    assert nv.nvfp4_quantize(A16, rows, cols, mode, iters, A16, A16, A16, None) == expect
+
+
+def test_quantize_rejects_null_and_misaligned():
+    assert nv.nvfp4_quantize(None, 4, 16, 0, 0, A16, A16, A16, None) == INVALID
+    assert nv.nvfp4_quantize(A16, 4, 16, 0, 0, None, A16, A16, None) == INVALID
+    assert nv.nvfp4_quantize(A16, 4, 16, 0, 0, A16, None, A16, None) == INVALID
+    assert nv.nvfp4_quantize(A16, 4, 16, 0, 0, A16, A16, None, None) == INVALID
+    assert nv.nvfp4_quantize(A16 + 8, 4, 16, 0, 0, A16, A16, A16, None) == MISALIGNED
+    assert nv.nvfp4_quantize(A16, 4, 16, 0, 0, A16 + 2, A16, A16, None) == MISALIGNED
+    assert nv.nvfp4_quantize(A16, 4, 16, 0, 0, A16, A16, A16 + 1, None) == MISALIGNED
+
+
+def test_dequantize_and_encode_reject_bad_arguments():
+    assert nv.nvfp4_dequantize(A16, A16, A16, 4, 24, A16, None) == INVALID
+    assert nv.nvfp4_dequantize(None, A16, A16, 4, 16, A16, None) == INVALID
+    assert nv.nvfp4_dequantize(A16, A16, None, 4, 16, A16, None) == INVALID
+    assert nv.nvfp4_dequantize(A16, A16, A16, 4, 16, A16 + 4, None) == MISALIGNED
+    assert nv.nvfp4_dequantize(A16 + 1, A16, A16, 4, 16, A16, None) == MISALIGNED
+    assert nv.nvfp4_encode_e2m1(None, 5, A16, None) == INVALID
+    assert nv.nvfp4_encode_e4m3(A16, -1, A16, None) == INVALID
+    assert nv.nvfp4_encode_e4m3(A16 + 1, 3, A16, None) == MISALIGNED
+
+
+def test_binding_names_mirror_the_header():
+    for n in declared_functions():
+        assert callable(getattr(nv, n)), n

@@ -1,0 +1,97 @@
+"""Parity at the benchmark workloads' full sizes, in the same launch
+configuration the benchmark times.  The oracle computes alpha and every CJSO
+iteration on the whole tensor; where the per-block final pass is too slow on
+the CPU (decoupled search, the 8192x28672 tensor) it is computed for a seeded
+sample of blocks, including the first and last block."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from gpu_util import block_mismatch, gpu_dequantize, gpu_quantize
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 8
+
+
+def sample_blocks(nblocks, n=20000, seed=0):
+    rng = np.random.default_rng(seed)
+    s = rng.choice(nblocks, size=min(n, nblocks), replace=False)
+    return np.unique(np.concatenate([s, [0, nblocks - 1]])).astype(np.int64)
+
+
+def check_full(w, mode, iters):
+    gc, gs, ga = gpu_quantize(w, mode, iters)
+    oc, os_, oa = oracle.quantize(w, mode, iters, threads=THREADS)
+    assert ga == oa
+    bad = block_mismatch(gc, gs, oc, os_)
+    if mode in (oracle.MAX, oracle.FOUR_OVER_SIX):
+        assert not bad.any(), bad.sum()
+    else:
+        assert bad.sum() <= int(1e-6 * bad.size), (bad.sum(), bad.size)
+        mg, mo = oracle.mse(w, gc, gs, ga), oracle.mse(w, oc, os_, oa)
+        assert abs(mg - mo) <= 1e-6 * mo
+    return gc, gs, ga
+
+
+def check_sampled(w, mode, iters, nsample=20000):
+    gc, gs, ga = gpu_quantize(w, mode, iters)
+    nb = w.size // 16
+    blocks = sample_blocks(nb, nsample, seed=mode * 100 + iters)
+    oc, os_, oa = oracle.quantize_sampled(w, mode, iters, blocks, threads=THREADS)
+    assert ga == oa
+    g8 = gc.reshape(-1, 8)[blocks]
+    gsc = gs.reshape(-1)[blocks]
+    bad = block_mismatch(g8, gsc, oc, os_)
+    assert bad.sum() <= int(1e-6 * nb), (bad.sum(), len(blocks))
+    return gc, gs, ga
+
+
+@pytest.fixture(scope="module")
+def studentt_4k():
+    return synthetic.studentt_4k()
+
+
+@pytest.fixture(scope="module")
+def mlp_up():
+    return synthetic.mlp_up()
+
+
+@pytest.mark.parametrize("mode", [oracle.MAX, oracle.FOUR_OVER_SIX])
+def test_studentt_4k_full(studentt_4k, mode):
+    """4096x4096 Student-t df=4 with outlier columns: max rule and FourOverSix."""
+    check_full(studentt_4k, mode, 0)
+
+
+@pytest.mark.parametrize("mode,iters", [(oracle.MAX, 0), (oracle.FOUR_OVER_SIX, 0), (oracle.CJSO, 5)])
+def test_mlp_up_full(mlp_up, mode, iters):
+    """4096x14336 row mixture: every block compared."""
+    gc, gs, ga = check_full(mlp_up, mode, iters)
+    if mode == oracle.MAX:
+        rows = slice(0, 64)
+        od = oracle.dequantize(gc[rows], gs[rows], ga, 64, mlp_up.shape[1])
+        assert np.array_equal(gpu_dequantize(gc, gs, ga, *mlp_up.shape)[rows], od)
+
+
+def test_mlp_up_decoupled_sampled(mlp_up):
+    check_sampled(mlp_up, oracle.CJSO_DECOUPLED, 5)
+
+
+@pytest.mark.parametrize("mode,iters", [(oracle.MAX, 0), (oracle.FOUR_OVER_SIX, 0), (oracle.CJSO, 5),
+                                        (oracle.CJSO_DECOUPLED, 5)])
+def test_mlp_70b_sampled(mode, iters):
+    """8192x28672 N(0, 0.01) with +-U(0.3, 1) spikes (larger than L2)."""
+    w = synthetic.mlp_70b()
+    check_sampled(w, mode, iters, nsample=20000 if mode != oracle.CJSO_DECOUPLED else 4000)
+
+
+@pytest.mark.parametrize("index", [0, 1, 4, 6, 223])
+def test_llama3_8b_tensors(index):
+    """Tensors of the 224-tensor Llama-3-8B-shaped stack (each its own alpha):
+    FourOverSix in full, decoupled CJSO on sampled blocks."""
+    w = synthetic.llama3_8b_tensor(index)
+    check_full(w, oracle.FOUR_OVER_SIX, 0)
+    check_sampled(w, oracle.CJSO_DECOUPLED, 5, nsample=3000)
