@@ -123,6 +123,37 @@ int nvfp4_encode_e2m1(const float *v, int64_t n, uint8_t *out, cudaStream_t stre
 int nvfp4_encode_e4m3(const float *v, int64_t n, uint8_t *out, cudaStream_t stream);
 
 /*
+ * nvfp4_quantize_noalloc -- the max rule or FourOverSix (mode 0 or 1 only),
+ *   with results identical to nvfp4_quantize, for callers that cannot let the
+ *   library allocate device memory: serving engines that reserve nearly all
+ *   device memory up front and account for every byte themselves,
+ *   latency-critical threads that must never enter an allocator (it can
+ *   block or reach the driver), and embedders whose own allocator must stay
+ *   the only one in the process.  The method's pages have no counterpart:
+ *   this is a deployment variant of the same computation.
+ * It calls no cudaMalloc/cudaFree or any allocating routine.  Its scratch is a
+ *   static device array of NVFP4_NOALLOC_SCRATCH_BYTES (16 KiB) that every GPU
+ *   which loads the library holds until the process exits.
+ * Limits and sharing:
+ *   - rows*cols <= NVFP4_NOALLOC_MAX_ELEMS (2^28): one scratch slot per 65,536
+ *     elements; larger tensors return NVFP4_ERR_INVALID_ARG before anything
+ *     is enqueued.
+ *   - Every call uses the same array.  Each call writes every slot it reads
+ *     before reading it, so nothing needs clearing between calls, but calls
+ *     that overlap on the GPU (e.g. on two streams) race on it and give wrong
+ *     results: serialize them.
+ *   - The first call on a device performs a one-time set-up with that device
+ *     current (it looks up the array's device address); make that first call
+ *     before any stream capture.
+ * Arguments, layouts, alignment and the other statuses are those of
+ * nvfp4_quantize (without `iters`).
+ */
+#define NVFP4_NOALLOC_SCRATCH_BYTES 16384
+#define NVFP4_NOALLOC_MAX_ELEMS (INT64_C(1) << 28)
+int nvfp4_quantize_noalloc(const void *W, int64_t rows, int64_t cols, int mode, uint8_t *codes,
+                           uint8_t *scales, float *alpha, cudaStream_t stream);
+
+/*
  * Kernel tracing.  While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on the stream it is launched on, so
  * per-kernel device time can be read back without an external profiler.

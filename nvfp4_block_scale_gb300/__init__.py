@@ -49,6 +49,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_encode_e2m1.restype = ci
     L.nvfp4_encode_e4m3.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e4m3.restype = ci
+    L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp]
+    L.nvfp4_quantize_noalloc.restype = ci
     L.nvfp4_profiler_enable.argtypes = [ci]
     L.nvfp4_profiler_enable.restype = ci
     L.nvfp4_profiler_reset.argtypes = []
@@ -72,6 +74,12 @@ def library_path() -> str:
 
 def nvfp4_quantize(W, rows, cols, mode, iters, codes, scales, alpha, stream) -> int:
     return load().nvfp4_quantize(W, rows, cols, mode, iters, codes, scales, alpha, stream)
+
+
+def nvfp4_quantize_noalloc(W, rows, cols, mode, codes, scales, alpha, stream) -> int:
+    """Allocation-free max-rule / FourOverSix quantize (see include/nvfp4.h):
+    for callers that must not let the library allocate device memory."""
+    return load().nvfp4_quantize_noalloc(W, rows, cols, mode, codes, scales, alpha, stream)
 
 
 def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
