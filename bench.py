@@ -1,24 +1,25 @@
 """Benchmark: NVFP4 quantize throughput (GB/s of bf16 input) on one GB300.
 
-Workload (default): the 4096x4096 bf16 Student-t (df=4, std 0.02) tensor with
+Headline workload: the 4096x4096 bf16 Student-t (df=4, std 0.02) tensor with
 0.1 % outlier columns x20; one step = quantize it with the max rule and with
-FourOverSix (the two scale rules this workload is quoted on).  Eight device
-copies of the input rotate (256 MiB > L2), so every step starts from HBM.
+FourOverSix (the two scale rules this workload is quoted on).  Enough device
+copies of the input rotate (> 2x L2) that every step starts from HBM.
 
-    python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--modes-table]
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+                    [--workload NAME --modes a,b --iters T] [--quick]
 
-One JSON line on stdout (rank 0).  `value` = bf16 input bytes of all ranks'
-steps / device time of the K steps (CUDA graph replays of the public C-ABI
-call sequence, CUDA events on the launching stream, barrier + synchronize on
-both sides, max over ranks).  `e2e` = the same metric through the C ABI with
-pinned host buffers (H2D of W and D2H of codes/scales/alpha inside the timed
-region).  `roofline` = the FourOverSix quantize call (its two kernels, timed
-with the library's per-launch CUDA events) against the measured HBM copy
-bandwidth.  `cpu_baseline` = the C oracle on the host cores.
+Prints one JSON line (rank 0).  `value` = bf16 input bytes of all ranks'
+steps / device time of the K steps (CUDA-graph replays of the C-ABI call
+sequence; CUDA events on the launching stream; barrier + synchronize on both
+sides; max over ranks).  `per_mode` = each mode alone, with per-kernel device
+times from the library's own per-launch CUDA events.  `roofline` = the
+heaviest mode of the step against its bound (HBM copy bandwidth, or the fp32
+pipe for the decoupled search).  `e2e` = the same metric through the C ABI with
+pinned host buffers (H2D of W, D2H of codes/scales/alpha inside the timed
+region).  `cpu_baseline` = the C oracle on the host cores (rank 0, N=1).
 
---impl reference runs the C oracle (the CPU restatement of the method) on a
-bounded sample of the same workload per step and prints the same line with
-"impl": "reference".
+--impl reference runs the C oracle on a bounded sample of the same workload
+per step and prints the same line with "impl": "reference".
 """
 from __future__ import annotations
 
@@ -39,11 +40,49 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
-WORKLOAD = "studentt_4k"
-WORKLOAD_DESC = "4096x4096 bf16, Student-t df=4 std 0.02, 0.1% columns x20 (seed 1 + rank); max + four_over_six"
-MODES = (("max", 0), ("four_over_six", 1))
-BYTES_PER_ELEM_ONE_PASS = 2.5625   # read W once (2) + codes (0.5) + scales (1/16)
-BYTES_PER_ELEM_TWO_PASS = 4.5625   # W read twice (alpha needs the global max first)
+HEADLINE = "studentt_4k"
+MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3}
+
+
+def _synth():
+    import synthetic
+    return synthetic
+
+
+# name -> (generator(rank), description, default modes)
+WORKLOADS = {
+    "studentt_4k": (lambda r: _synth().studentt_4k(seed=1 + r),
+                    "4096x4096 bf16, Student-t df=4 std 0.02, 0.1% columns x20 (seed 1 + rank)",
+                    ("max", "four_over_six")),
+    "gauss_1k": (lambda r: _synth().gauss_1k(seed=0 + r),
+                 "1024x1024 bf16, N(0,0.02) (seed 0 + rank)", ("max", "four_over_six", "cjso", "cjso_decoupled")),
+    "mlp_up": (lambda r: _synth().mlp_up(seed=2 + r),
+               "4096x14336 bf16, 10% rows N(0,0.05), rest N(0,0.015) (seed 2 + rank)",
+               ("max", "four_over_six", "cjso", "cjso_decoupled")),
+    "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
+                "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)",
+                ("max", "four_over_six", "cjso", "cjso_decoupled")),
+}
+
+ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
+TWO_PASS = 4.5625   # B/elem: W read twice (alpha needs the global max first)
+DECOUPLED_FLOPS = 101 * 9  # per element: 101 candidates x (quotient 5 + P, R 4) fp32 flops
+
+
+def kernels_per_call(mode: int, iters: int) -> int:
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters}[mode]
+
+
+def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
+    """(bound, unit, algorithmic work of one call, rule) for a mode."""
+    fits = 2 * n <= l2_bytes // 2
+    if mode in (0, 1):
+        b = ONE_PASS if fits else TWO_PASS
+        return "hbm", "GB/s", b * n, f"{b} B/elem ({'W <= L2/2: one HBM read' if fits else 'W read twice'})"
+    if mode == 2:
+        b = ONE_PASS if fits else (iters + 2) * 2 + 0.5625
+        return "hbm", "GB/s", b * n, f"{b} B/elem ({'W stays in L2' if fits else f'{iters + 2} reads of W'})"
+    return "alu", "TFLOP/s", DECOUPLED_FLOPS * n, "909 fp32 flop/elem (101 candidates x 9)"
 
 
 # --------------------------------------------------------------------------- clocks
@@ -122,6 +161,11 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def fp32_peak_tflops(sms: int, mhz: float) -> float:
+    """FP32 FMA peak: SMs x 128 lanes x 2 flop x clock."""
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scale_gb300", "csrc")
@@ -130,54 +174,51 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the
+def recorded_traffic(key: str):
+    """DRAM bytes per call from the committed ncu summary, if taken on the
     current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        d = json.load(open(p))
-        e = d[kernel_key]
+        e = json.load(open(p))[key]
         if e.get("source_digest") == source_digest():
-            return e["dram_bytes_per_launch"]
+            return e["dram_bytes_per_call"]
     except Exception:
         pass
     return None
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def oracle_cpu_baseline(w_bits, min_seconds=2.0):
-    """The oracle as it stands, all host cores, full tensor, both modes."""
+def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=2.0, max_rows=None):
+    """The oracle as it stands on all host cores; the first `max_rows` rows."""
     import oracle
     threads = os.cpu_count() or 1
+    sample = w_bits if max_rows is None else w_bits[:max_rows]
     t0 = time.perf_counter()
     reps = 0
     while True:
-        for _, m in MODES:
-            oracle.quantize(w_bits, m, 0, threads=threads)
+        for m in modes:
+            oracle.quantize(sample, MODE_IDS[m], iters, threads=threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
             break
-    gbs = reps * len(MODES) * w_bits.nbytes / el / 1e9
+    gbs = reps * len(modes) * sample.nbytes / el / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"full {w_bits.shape[0]}x{w_bits.shape[1]} tensor, max + four_over_six, {reps} repetition(s), "
-                      f"{el:.1f} s"}
+            "sample": f"rows 0..{sample.shape[0] - 1} of {w_bits.shape[0]}x{w_bits.shape[1]}, "
+                      f"{'+'.join(modes)}, {reps} repetition(s) in {el:.1f} s"}
 
 
 # --------------------------------------------------------------------------- our arm
 
-def run_ours(args):
+def run_ours(args, modes):
     import torch
     import torch.distributed as dist
 
     import nvfp4_block_scale_gb300 as nv
-    import synthetic
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -185,48 +226,58 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-
-    w_bits = synthetic.studentt_4k(seed=1 + rank)
+    make, desc, _ = WORKLOADS[args.workload]
+    w_bits = make(rank)
     rows, cols = w_bits.shape
     n = w_bits.size
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ncopy = max(8, math.ceil(2 * l2 / w_bits.nbytes))
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    ncopy = max(2, min(8, math.ceil(2 * l2 / w_bits.nbytes) + 1))
     W_host = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16)
     Wd = [W_host.to(dev) for _ in range(ncopy)]
+    mids = [MODE_IDS[m] for m in modes]
     outs = {m: (torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
-                torch.empty(1, dtype=torch.float32, device=dev)) for _, m in MODES}
+                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids}
 
     def call(mode, w, s):
         c, sc, a = outs[mode]
-        st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, 0, c.data_ptr(), sc.data_ptr(), a.data_ptr(),
-                               s.cuda_stream)
+        st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
+                               a.data_ptr(), s.cuda_stream)
         if st != 0:
             raise RuntimeError(f"nvfp4_quantize: {nv.nvfp4_status_string(st)}")
 
     def step(i, s):
-        for j, (_, m) in enumerate(MODES):
-            call(m, Wd[(i * len(MODES) + j) % ncopy], s)
+        for j, m in enumerate(mids):
+            call(m, Wd[(i * len(mids) + j) % ncopy], s)
 
     for i in range(max(args.warmup, 3)):
         step(i, stream)
     torch.cuda.synchronize()
 
-    # CUDA graphs: one per rotation slot, each = one step (both modes).
-    launch = "cuda_graph"
+    launch = "eager"
     graphs = []
-    try:
-        for i in range(ncopy):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                step(i, torch.cuda.current_stream())
-            graphs.append(g)
-        for g in graphs:
-            g.replay()
-        torch.cuda.synchronize()
-    except Exception as e:  # eager fallback, reported in config
-        launch = f"eager ({type(e).__name__})"
-        graphs = []
+    if not args.quick:  # one CUDA graph per rotation slot, each = one step
+        try:
+            for i in range(ncopy):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step(i, torch.cuda.current_stream())
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+            launch = "cuda_graph"
+        except Exception as e:  # eager fallback, reported in config
+            launch = f"eager ({type(e).__name__})"
+            graphs = []
+
+    def run_steps(k, s):
+        for i in range(k):
+            if graphs:
+                graphs[i % len(graphs)].replay()
+            else:
+                step(i, s)
 
     def timed(k):
         if ws > 1:
@@ -235,11 +286,7 @@ def run_ours(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(k):
-            if graphs:
-                graphs[i % ncopy].replay()
-            else:
-                step(i, stream)
+        run_steps(k, stream)
         e1.record(stream)
         torch.cuda.synchronize()
         if ws > 1:
@@ -248,69 +295,100 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     for attempt in range(2):
-        for i in range(max(args.warmup, 3)):
-            (graphs[i % ncopy].replay() if graphs else step(i, stream))
+        run_steps(max(args.warmup, 3), stream)
         clocks.start()
         ms = timed(args.steps)
-        if len(clocks.samples) < 5:  # short timed region: keep sampling over the same loop
+        if len(clocks.samples) < 5 and not args.quick:  # short region: keep sampling over the same loop
             timed(max(args.steps, int(200.0 / max(ms / args.steps, 1e-3))))
         clocks.stop()
         csum = clocks.summary()
         if not (set(csum.get("reasons", [])) & BAD_REASONS):
             break
+        csum["remeasured"] = True
     ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
     if ws > 1:
         dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
     ms = float(ms_t.item())
-    ms_per_step = ms / args.steps
-    bytes_per_step = len(MODES) * 2 * n
+    bytes_per_step = len(mids) * 2 * n
     value = ws * bytes_per_step * args.steps / (ms / 1e3) / 1e9
+    out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
+           "config": {"workload": args.workload, "desc": desc, "rows": rows, "cols": cols, "modes": list(modes),
+                      "cjso_iters": args.iters if any(m >= 2 for m in mids) else None,
+                      "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB)",
+                      "launch": launch, "parallelism": f"{ws} independent replica(s), one tensor per rank"},
+           "gpu_launches": sum(kernels_per_call(m, args.iters) for m in mids) * args.steps, "clocks": csum}
+    if args.quick:
+        if ws > 1:
+            dist.destroy_process_group()
+        return out if rank == 0 else None
 
-    # per-mode device throughput and per-kernel times (library CUDA events)
+    # ---- per mode: device throughput and per-kernel times (library CUDA events)
     per_mode = {}
-    for name, m in MODES:
-        nv.nvfp4_profiler_reset()
-        nv.nvfp4_profiler_enable(1)
-        k = max(args.steps, 20)
+    peak_hbm, peak_kind = measured_peaks()
+    sm_mhz = csum.get("sm_mhz") or 1900.0
+    for name, m in zip(modes, mids):
+        # device time of this mode alone: graph replays of one call per rotation slot
+        k = max(min(args.steps, 500), 20)
+        gm = []
+        if graphs:
+            for i in range(ncopy):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    call(m, Wd[i], torch.cuda.current_stream())
+                gm.append(g)
+        for i in range(ncopy):
+            (gm[i].replay() if gm else call(m, Wd[i], stream))
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(k):
-            call(m, Wd[i % ncopy], stream)
+            (gm[i % ncopy].replay() if gm else call(m, Wd[i % ncopy], stream))
         e1.record(stream)
+        torch.cuda.synchronize()
+        call_ms = e0.elapsed_time(e1) / k
+        # per-kernel breakdown from the library tracer (event-bracketed launches,
+        # so each includes its launch gap)
+        nv.nvfp4_profiler_reset()
+        nv.nvfp4_profiler_enable(1)
+        for i in range(20):
+            call(m, Wd[i % ncopy], stream)
         torch.cuda.synchronize()
         nv.nvfp4_profiler_enable(0)
         rep = nv.profiler_report()
-        kern_ms = sum(v[1] for v in rep.values()) / k
-        per_mode[name] = {"GBps_bf16_in": 2 * n / (kern_ms / 1e3) / 1e9, "us_per_call_kernels": kern_ms * 1e3,
-                          "us_per_call_eager_wall": e0.elapsed_time(e1) / k * 1e3,
-                          "kernels": {kn: {"launches": c, "avg_us": t / c * 1e3} for kn, (c, t) in rep.items()}}
+        bound, unit, work, rule = algorithmic(m, args.iters, n, l2)
+        if bound == "hbm":
+            achieved, peak, pk = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind
+        else:
+            achieved = work / (call_ms / 1e3) / 1e12
+            peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
+        per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "us_per_call": call_ms * 1e3,
+                          "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule},
+                          "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
+                                                      for kn, (c, t) in rep.items()}}
+    heavy = max(per_mode, key=lambda k: per_mode[k]["us_per_call"])
+    hr = per_mode[heavy]["roofline"]
+    out["per_mode"] = per_mode
+    out["roofline"] = {"bound": hr["bound"], "achieved": hr["achieved"], "peak": hr["peak"], "unit": hr["unit"],
+                       "frac": hr["frac"],
+                       "traffic": recorded_traffic(f"nvfp4_quantize({heavy})@{args.workload}"),
+                       "kernel": f"nvfp4_quantize({heavy}) = "
+                                 + " + ".join(per_mode[heavy]["kernels_event_bracketed"]),
+                       "peak_kind": hr["peak_kind"], "rule": hr["rule"],
+                       "timing": "CUDA events on the launching stream around CUDA-graph replays of the call "
+                                 "alone (its kernels back to back)"}
 
-    peak, peak_kind = measured_peaks()
-    fos = per_mode["four_over_six"]
-    call_s = fos["us_per_call_kernels"] / 1e6
-    alg_bytes = BYTES_PER_ELEM_ONE_PASS * n
-    achieved = alg_bytes / call_s / 1e9
-    traffic = recorded_traffic("nvfp4_quantize(four_over_six)@studentt_4k")
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_kind": peak_kind,
-                "kernel": "nvfp4_quantize(four_over_six) = k_amax_partials + k_quant_max_fos<fos>",
-                "algorithmic_bytes_per_launch": alg_bytes,
-                "bytes_rule": "2.5625 B/elem: W read once, codes 0.5, scales 1/16 (W fits in L2, second read hits L2)"}
-    for name in per_mode:
-        per_mode[name]["frac_of_hbm_one_pass"] = (BYTES_PER_ELEM_ONE_PASS * n / (per_mode[name]["us_per_call_kernels"] / 1e6) / 1e9) / peak
-
-    # end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers
     W_pin = W_host.pin_memory()
     Wd0 = torch.empty_like(Wd[0])
-    host_outs = {m: (torch.empty((rows, cols // 2), dtype=torch.uint8).pin_memory(),
-                     torch.empty((rows, cols // 16), dtype=torch.uint8).pin_memory(),
-                     torch.empty(1, dtype=torch.float32).pin_memory()) for _, m in MODES}
+    host_outs = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m]) for m in mids}
 
     def e2e_step():
         Wd0.copy_(W_pin, non_blocking=True)
-        for _, m in MODES:
+        for m in mids:
             call(m, Wd0, stream)
             for dst, src in zip(host_outs[m], outs[m]):
                 dst.copy_(src, non_blocking=True)
@@ -322,7 +400,7 @@ def run_ours(args):
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    k_e2e = max(args.steps // 4, 5)
+    k_e2e = max(min(args.steps // 4, 200), 5)
     e0.record(stream)
     for _ in range(k_e2e):
         e2e_step()
@@ -332,42 +410,34 @@ def run_ours(args):
     if ws > 1:
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     d2h = sum(t.numel() * t.element_size() for m in host_outs for t in host_outs[m])
-    e2e = {"value": ws * bytes_per_step * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e}
+    out["e2e"] = {"value": ws * bytes_per_step * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
+                  "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e}
 
-    out = None
-    if rank == 0:
-        cpu = oracle_cpu_baseline(w_bits) if ws == 1 else None
-        out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-               "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "bf16->nvfp4 (fp32 arithmetic)", "data": "synthetic",
-               "config": {"workload": WORKLOAD, "desc": WORKLOAD_DESC, "rows": rows, "cols": cols,
-                          "modes": [m for m, _ in MODES], "l2": f"rotate {ncopy} input copies "
-                          f"({ncopy * w_bits.nbytes >> 20} MiB > 2x L2 {l2 >> 20} MiB)", "launch": launch,
-                          "parallelism": f"{ws} independent replicas (one tensor per rank, no collective)"},
-               "per_mode": per_mode, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-               "gpu_launches": 2 * len(MODES) * args.steps, "clocks": csum}
+    if rank == 0 and ws == 1:
+        rows_cap = None if n <= (1 << 24) else max(16, (1 << 22) // cols)
+        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, modes, args.iters, max_rows=rows_cap)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
-    return out
+    return out if rank == 0 else None
 
 
 # --------------------------------------------------------------------------- reference arm
 
-def run_reference(args):
+def run_reference(args, modes):
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
     import oracle
-    import synthetic
-    w_bits = synthetic.studentt_4k(seed=1)
-    sample = w_bits[:512]  # bounded per-step sample: 512 of the 4096 rows
+    make, desc, _ = WORKLOADS[args.workload]
+    w_bits = make(0)
+    rows = max(16, min(w_bits.shape[0], (1 << 21) // w_bits.shape[1]))
+    sample = w_bits[:rows]  # bounded per-step sample of the workload
     threads = os.cpu_count() or 1
 
     def step():
-        for _, m in MODES:
-            oracle.quantize(sample, m, 0, threads=threads)
+        for m in modes:
+            oracle.quantize(sample, MODE_IDS[m], args.iters, threads=threads)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -375,15 +445,16 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = len(MODES) * sample.nbytes * args.steps / el / 1e9
-    desc = f"C oracle, {threads} host threads, rows 0..511 of the 4096x4096 tensor per step, max + four_over_six"
+    value = len(modes) * sample.nbytes * args.steps / el / 1e9
+    sdesc = (f"C oracle, {threads} host threads, rows 0..{rows - 1} of the {w_bits.shape[0]}x{w_bits.shape[1]} "
+             f"tensor per step, {'+'.join(modes)}")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16->nvfp4 (fp32 arithmetic)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "desc": WORKLOAD_DESC, "rows": 4096, "cols": 4096,
-                       "modes": [m for m, _ in MODES]},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+            "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": desc, "rows": int(w_bits.shape[0]),
+                       "cols": int(w_bits.shape[1]), "modes": list(modes)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sdesc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -393,11 +464,17 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
+    ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
-    if args.impl == "reference":
-        out = run_reference(args)
-    else:
-        out = run_ours(args)
+    modes = tuple(args.modes.split(",")) if args.modes else WORKLOADS[args.workload][2]
+    for m in modes:
+        if m not in MODE_IDS:
+            raise SystemExit(f"unknown mode {m}")
+    out = run_reference(args, modes) if args.impl == "reference" else run_ours(args, modes)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -105,9 +105,9 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
        kTrKinds };
-const char *const kTraceNames[kTrKinds] = {"k_amax_partials",   "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
-                                           "k_cjso_sweep<init>", "k_cjso_sweep<iter>",   "k_decoupled",
-                                           "k_dequant",          "k_encode"};
+const char *const kTraceNames[kTrKinds] = {"k_amax_partials",    "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
+                                           "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
+                                           "k_dequant",           "k_encode"};
 
 struct TraceRec {
   int kind;
@@ -185,8 +185,8 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int64_t H = n / 8;   // half blocks = 16-byte loads
   const int64_t B = n / 16;  // blocks
   const int T = cjso ? iters : 0;
-  const int g_amax = grid_for(*d, kKernAmax, H / 4 + 1);
-  const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, H);
+  const int g_amax = grid_for(*d, kKernAmax, H / 8 + 1);  // 8 loads per thread per tile
+  const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, H);
   const int g_dec = grid_for(*d, kKernDecoupled, B);
 

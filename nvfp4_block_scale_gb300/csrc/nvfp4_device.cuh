@@ -122,6 +122,222 @@ __device__ __forceinline__ void unpack8(const uint4 &w, float (&ax)[8], uint32_t
   }
 }
 
+// ---------------------------------------------------------------------------
+// Packed primitives for one 16-element block held by one thread.
+// ---------------------------------------------------------------------------
+
+typedef unsigned long long f32x2;  // two fp32 in one 64-bit register: {lo, hi}
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// -fl(x / s) for both lanes of a signed pair (Markstein step of div_by_scale
+// with negated operands, nr = -r): nq = fl(-x*r), e = fl(x + nq*s) (the exact
+// remainder), w = fl(e*nr + nq) = -fl(x/s).  Negation commutes with
+// round-to-nearest, so w is exactly the negated IEEE quotient, and the signs
+// of zeros come out right: w = -(+-0) for x = +-0, and for s = 0 (r = 0)
+// w = -(+-0) with the sign of x.  Callers encode w and flip the code signs.
+__device__ __forceinline__ f32x2 negdiv2_by_scale(f32x2 x, f32x2 s, f32x2 nr) {
+  f32x2 nq = mul2(x, nr);
+  f32x2 e = fma2(nq, s, x);
+  return fma2(e, nr, nq);
+}
+
+// One 16-element block: the signed weights as fp32 pairs (for the quotients)
+// and as f16 pairs scaled by 2^sh (for P; exact for every element whose code
+// is nonzero, see quant16).  x[k] / xh[k] hold elements 2k (lo) and 2k+1 (hi).
+struct Block16 {
+  f32x2 x[8];
+  uint32_t xh[8];
+  float p_unscale;  // 2^-sh
+};
+
+// Signed E2M1 codes of 8 quotients (4 pairs) packed into one word (element
+// 2k in the low nibble of byte k).
+__device__ __forceinline__ uint32_t encode8(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+      "mov.b64 {a0, b0}, %1;\n\tmov.b64 {a1, b1}, %2;\n\tmov.b64 {a2, b2}, %3;\n\tmov.b64 {a3, b3}, %4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r) : "l"(v0), "l"(v1), "l"(v2), "l"(v3));
+  return r;
+}
+
+// As encode8, and also accumulates P += sum x' q (mixed f16 x f16 -> f32
+// fma, exact) and R2 += q^2 (f16x2, exact for up to 8 terms per lane).
+__device__ __forceinline__ uint32_t encode8_sums(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, uint32_t h0,
+                                                 uint32_t h1, uint32_t h2, uint32_t h3, float &P,
+                                                 uint32_t &R2) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+      ".reg .b32 q0, q1, q2, q3;\n\t.reg .f16 ql, qh, xl, xh;\n\t"
+      "mov.b64 {a0, b0}, %3;\n\tmov.b64 {a1, b1}, %4;\n\tmov.b64 {a2, b2}, %5;\n\tmov.b64 {a3, b3}, %6;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t"
+      "cvt.rn.f16x2.e2m1x2 q0, t0;\n\tcvt.rn.f16x2.e2m1x2 q1, t1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 q2, t2;\n\tcvt.rn.f16x2.e2m1x2 q3, t3;\n\t"
+      "fma.rn.f16x2 %2, q0, q0, %2;\n\tfma.rn.f16x2 %2, q1, q1, %2;\n\t"
+      "fma.rn.f16x2 %2, q2, q2, %2;\n\tfma.rn.f16x2 %2, q3, q3, %2;\n\t"
+      "mov.b32 {ql, qh}, q0;\n\tmov.b32 {xl, xh}, %7;\n\t"
+      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
+      "mov.b32 {ql, qh}, q1;\n\tmov.b32 {xl, xh}, %8;\n\t"
+      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
+      "mov.b32 {ql, qh}, q2;\n\tmov.b32 {xl, xh}, %9;\n\t"
+      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
+      "mov.b32 {ql, qh}, q3;\n\tmov.b32 {xl, xh}, %10;\n\t"
+      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t}"
+      : "=r"(r), "+f"(P), "+r"(R2)
+      : "l"(v0), "l"(v1), "l"(v2), "l"(v3), "r"(h0), "r"(h1), "r"(h2), "r"(h3));
+  return r;
+}
+
+// f16x2 -> sum of both halves in fp32 (exact for the small integers/4 of R).
+__device__ __forceinline__ float f16x2_sum(uint32_t h) {
+  __half2 v = *reinterpret_cast<__half2 *>(&h);
+  float2 f = __half22float2(v);
+  return __fadd_rn(f.x, f.y);
+}
+
+// Loads of one block: 2 x 16 bytes -> Block16 (signed fp32 pairs, scaled f16
+// pairs) and the block's max |x| as bf16 bits.  `need_h`: build xh (only the
+// error-comparing rules need P).
+__device__ __forceinline__ uint32_t unpack16(const uint4 &a, const uint4 &b, Block16 &blk, bool need_h) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t m = w[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(w[k]));
+  m &= 0x7FFF7FFFu;
+  const uint32_t amax_bits = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) blk.x[k] = pack2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+  if (need_h) {
+    // 2^sh with sh = 4 - floor(log2 amax): |x| * 2^sh < 32 for the whole
+    // block, and >= 2^-14 (f16 normal, exact) for every |x| >= amax / 2^18.
+    int e = (int)(amax_bits >> 7);                 // bf16 exponent field
+    int se = min(max(127 + 131 - e, 1), 253);       // biased exponent of 2^sh
+    float sc = __uint_as_float((uint32_t)se << 23);
+    blk.p_unscale = __uint_as_float((uint32_t)(254 - se) << 23);
+    f32x2 sc2 = pack2(sc, sc);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      f32x2 y = mul2(blk.x[k], sc2);
+      float lo, hi;
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y));
+      __half2 hh = __floats2half2_rn(lo, hi);
+      blk.xh[k] = *reinterpret_cast<uint32_t *>(&hh);
+    }
+  }
+  return amax_bits;
+}
+
+// Quantizes a block with dequant scale s (reciprocal r): signed codes of
+// elements 0-7 / 8-15 in c0 / c1; with `sums`, P = sum |x| q and R = sum q^2
+// (both exact).  A zero scale (r = 0) gives sign-only codes and zero sums.
+// The quotients are computed negated (negdiv2_by_scale): encoding -v gives
+// the codes with every sign bit flipped and P with its sign flipped; both
+// are undone once per word / block.
+template <bool SUMS>
+__device__ __forceinline__ void quant16(const Block16 &blk, float s, float r, uint32_t &c0, uint32_t &c1,
+                                        float &P, float &R) {
+  const f32x2 s2 = pack2(s, s), nr2 = pack2(-r, -r);
+  f32x2 w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) w[k] = negdiv2_by_scale(blk.x[k], s2, nr2);
+  if (SUMS) {
+    float p = 0.0f;
+    uint32_t r2h = 0u;
+    c0 = encode8_sums(w[0], w[1], w[2], w[3], blk.xh[0], blk.xh[1], blk.xh[2], blk.xh[3], p, r2h);
+    c1 = encode8_sums(w[4], w[5], w[6], w[7], blk.xh[4], blk.xh[5], blk.xh[6], blk.xh[7], p, r2h);
+    P = __fmul_rn(p, -blk.p_unscale);  // sum of x' * (-q) -> sum |x| q
+    R = f16x2_sum(r2h);
+  } else {
+    c0 = encode8(w[0], w[1], w[2], w[3]);
+    c1 = encode8(w[4], w[5], w[6], w[7]);
+  }
+  c0 ^= 0x88888888u;
+  c1 ^= 0x88888888u;
+}
+
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled now / wait until the previous kernel's writes are visible.  Both
+// are no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Bulk (TMA) copies into shared memory, tracked by mbarriers.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+// Makes initialized mbarriers visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later bulk-copy writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// One thread: expect `bytes` on `bar` and start the copy global -> shared.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Waits for phase `parity` of `bar` to complete, giving up after `limit`
+// polls.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Compensated (float, float) accumulator, ~48 significant bits.
 struct FF {
   float hi, lo;

@@ -107,35 +107,38 @@ __device__ __forceinline__ uint4 load_half(const uint4 *__restrict__ W, int64_t 
 // a1: global amax partials
 // ---------------------------------------------------------------------------
 
+// Each CTA walks tiles of kThreads * kAmaxUnroll 16-byte units (all loads of
+// a tile in flight at once), keeps max |x| as a bf16 pair, and writes one
+// partial.  Launched as a programmatic dependent of whatever precedes it on
+// the stream, it waits for that grid before touching W, then lets the
+// quantize kernel be scheduled at once; that kernel waits for this grid's
+// completion before reading the partials.
+constexpr int kAmaxUnroll = 8;
+
 __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restrict__ W, int64_t n16,
                                                             uint32_t *__restrict__ part) {
   __shared__ uint32_t red[kWarps];
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
-  int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  __nv_bfloat162 m2 = __float2bfloat162_rn(0.0f);
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    uint4 a = __ldg(W + i), b = __ldg(W + i + stride), c = __ldg(W + i + 2 * stride),
-          d = __ldg(W + i + 3 * stride);
-    const uint32_t ws[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
-                             c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+  pdl_wait();  // W may be written by the previous kernel of the stream
+  pdl_launch_dependents();
+  uint32_t m = 0u;
+  const int64_t tile = (int64_t)kThreads * kAmaxUnroll;
+  for (int64_t base = (int64_t)blockIdx.x * tile + threadIdx.x; base < n16; base += (int64_t)gridDim.x * tile) {
+    uint4 v[kAmaxUnroll];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      uint32_t t = ws[k] & 0x7FFF7FFFu;
-      m2 = __hmax2(m2, *reinterpret_cast<__nv_bfloat162 *>(&t));
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kThreads;
+      v[u] = i < n16 ? __ldg(W + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].x));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].y));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].z));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].w));
     }
   }
-  for (; i < n16; i += stride) {
-    uint4 a = __ldg(W + i);
-    const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t t = ws[k] & 0x7FFF7FFFu;
-      m2 = __hmax2(m2, *reinterpret_cast<__nv_bfloat162 *>(&t));
-    }
-  }
-  uint32_t mb = *reinterpret_cast<uint32_t *>(&m2);
-  uint32_t m = max(mb & 0xFFFFu, mb >> 16);
-  m = block_max_u32(m, red);
+  m &= 0x7FFF7FFFu;
+  m = block_max_u32(max(m & 0xFFFFu, m >> 16), red);
   if (threadIdx.x == 0) part[blockIdx.x] = m;
 }
 
@@ -143,8 +146,13 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
 // a2-a4, a7: max rule and FourOverSix
 // ---------------------------------------------------------------------------
 
+// One 16-element block per thread, grid-stride, the next two blocks of the
+// thread in flight while one is computed.  Launched as a programmatic
+// dependent of k_amax_partials: W was final before that kernel read it, so
+// the first blocks are fetched before the wait.  It lets the next kernel of
+// the stream be scheduled early; that kernel waits for this one to finish.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restrict__ W, int64_t H,
+__global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restrict__ W, int64_t B,
                                                             const uint32_t *__restrict__ amax_part, int n_amax,
                                                             uint32_t *__restrict__ codes32,
                                                             uint8_t *__restrict__ scales,
@@ -152,46 +160,52 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
   __shared__ uint32_t red[kWarps];
   __shared__ float s_tab[128], r_tab[128];
   __shared__ uint8_t c4_tab[128];
+  constexpr bool FOS = MODE == kModeFourOverSix;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
+  const int64_t b1 = b + stride;
+  uint4 n0 = b1 < B ? __ldg(W + 2 * b1) : z, n1 = b1 < B ? __ldg(W + 2 * b1 + 1) : z;
+
+  pdl_launch_dependents();
+  pdl_wait();
   const float alpha = fold_alpha(amax_part, n_amax, red);
   if (blockIdx.x == 0 && threadIdx.x == 0) *alpha_out = alpha;
   const float six_a = __fmul_rn(alpha, 6.0f);
   const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
   build_scale_tables(alpha, s_tab, r_tab);
-  if (MODE == kModeFourOverSix && threadIdx.x < 128)  // [FOS-02] scale_m4 = fp8(scale_m6 * 1.5)
+  if (FOS && threadIdx.x < 128)  // [FOS-02] scale_m4 = fp8(scale_m6 * 1.5)
     c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(e4m3_value(threadIdx.x), 1.5f));
   __syncthreads();
 
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t base = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 32; base < H;
-       base += nwarps * 32) {
-    const int64_t h = base + lane;
-    const bool valid = h < H;
-    float ax[8];
-    uint32_t sgn, am;
-    unpack8(load_half(W, h, valid), ax, sgn, am);
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+  for (; b < B; b += stride) {
+    const int64_t b2 = b + 2 * stride;
+    const uint4 m0 = b2 < B ? __ldg(W + 2 * b2) : z, m1 = b2 < B ? __ldg(W + 2 * b2 + 1) : z;
+    Block16 blk;
+    const uint32_t am = unpack16(a0, a1, blk, FOS);
     const uint32_t d6 = max_rule_code(am, six_a, r6);
-    uint32_t d = d6, mags;
-    HalfQ q6 = quant_half(ax, s_tab[d6], r_tab[d6]);
-    if (MODE == kModeFourOverSix) {
+    uint32_t c0, c1, d = d6;
+    float P6, R6;
+    quant16<FOS>(blk, s_tab[d6], r_tab[d6], c0, c1, P6, R6);
+    if (FOS) {
       // [FOS-02] keep scale_m4 iff its dequant error is strictly lower.
       const uint32_t d4 = c4_tab[d6];
-      HalfQ q4 = quant_half(ax, s_tab[d4], r_tab[d4]);
-      const float P6 = __fadd_rn(q6.P, __shfl_xor_sync(0xFFFFFFFFu, q6.P, 1));
-      const float R6 = __fadd_rn(q6.R, __shfl_xor_sync(0xFFFFFFFFu, q6.R, 1));
-      const float P4 = __fadd_rn(q4.P, __shfl_xor_sync(0xFFFFFFFFu, q4.P, 1));
-      const float R4 = __fadd_rn(q4.R, __shfl_xor_sync(0xFFFFFFFFu, q4.R, 1));
+      uint32_t e0, e1;
+      float P4, R4;
+      quant16<true>(blk, s_tab[d4], r_tab[d4], e0, e1, P4, R4);
       const bool use4 = cand_err(s_tab[d4], P4, R4) < cand_err(s_tab[d6], P6, R6);
       d = use4 ? d4 : d6;
-      mags = use4 ? q4.mags : q6.mags;
-    } else {
-      mags = q6.mags;
+      c0 = use4 ? e0 : c0;
+      c1 = use4 ? e1 : c1;
     }
-    if (valid) {
-      codes32[h] = mags | sgn;
-      if (!(lane & 1)) scales[h >> 1] = (uint8_t)d;
-    }
+    codes32[2 * b] = c0;  // two 4-byte stores: codes is only 4-byte aligned
+    codes32[2 * b + 1] = c1;
+    scales[b] = (uint8_t)d;
+    a0 = n0;
+    a1 = n1;
+    n0 = m0;
+    n1 = m1;
   }
 }
 
@@ -412,17 +426,28 @@ cudaLaunchConfig_t make_cfg(int grid, cudaStream_t st) {
 
 cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_amax_partials, static_cast<const uint4 *>(W), n16, part);
 }
 
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const uint4 *w = static_cast<const uint4 *>(W);
   uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  const int64_t B = H / 2;
   if (mode == kModeFourOverSix)
-    return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeFourOverSix>, w, H, amax_part, n_amax, c, scales, alpha);
-  return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, H, amax_part, n_amax, c, scales, alpha);
+    return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeFourOverSix>, w, B, amax_part, n_amax, c, scales, alpha);
+  return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, B, amax_part, n_amax, c, scales, alpha);
 }
 
 cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,

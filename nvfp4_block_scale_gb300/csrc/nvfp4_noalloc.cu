@@ -119,7 +119,7 @@ extern "C" int nvfp4_quantize_noalloc(const void *W, int64_t rows, int64_t cols,
   // One amax CTA (one 4-byte slot) per 65,536 elements: at most 4096 slots.
   const int g_amax = (int)((n + kElemsPerAmaxCta - 1) / kElemsPerAmaxCta);
   if (g_amax > kNoAllocMaxCtas) return NVFP4_ERR_INVALID_ARG;
-  const int g_quant = na_grid(d->sms, mode == kModeFourOverSix ? d->occ_fos : d->occ_max, H);
+  const int g_quant = na_grid(d->sms, mode == kModeFourOverSix ? d->occ_fos : d->occ_max, n / 16);
   cudaError_t e = launch_amax_partials(W, H, d->scratch, g_amax, stream);
   if (e == cudaSuccess) e = launch_quant_max_fos(mode, W, H, d->scratch, g_amax, codes, scales, alpha, g_quant, stream);
   return na_map(e);
