@@ -158,13 +158,10 @@ __device__ __forceinline__ f32x2 negdiv2_by_scale(f32x2 x, f32x2 s, f32x2 nr) {
   return fma2(e, nr, nq);
 }
 
-// One 16-element block: the signed weights as fp32 pairs (for the quotients)
-// and as f16 pairs scaled by 2^sh (for P; exact for every element whose code
-// is nonzero, see quant16).  x[k] / xh[k] hold elements 2k (lo) and 2k+1 (hi).
+// One 16-element block: the signed weights as fp32 pairs; x[k] holds
+// elements 2k (lo) and 2k+1 (hi).
 struct Block16 {
   f32x2 x[8];
-  uint32_t xh[8];
-  float p_unscale;  // 2^-sh
 };
 
 // Signed E2M1 codes of 8 quotients (4 pairs) packed into one word (element
@@ -180,32 +177,30 @@ __device__ __forceinline__ uint32_t encode8(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 
   return r;
 }
 
-// As encode8, and also accumulates P += sum x' q (mixed f16 x f16 -> f32
-// fma, exact) and R2 += q^2 (f16x2, exact for up to 8 terms per lane).
-__device__ __forceinline__ uint32_t encode8_sums(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, uint32_t h0,
-                                                 uint32_t h1, uint32_t h2, uint32_t h3, float &P,
-                                                 uint32_t &R2) {
-  uint32_t r;
+// As encode8, and also accumulates the sums of the block: P2 += x * q over
+// the 4 pairs (fp32 pairs; products exact, sums exact by the range argument)
+// and R2 += q^2 (f16x2, exact for up to 8 terms per lane).  q is decoded
+// from the codes just produced (cvt f16x2 <- e2m1x2, then f16 -> f32).
+__device__ __forceinline__ uint32_t encode8_sums(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, f32x2 x0, f32x2 x1,
+                                                 f32x2 x2, f32x2 x3, f32x2 &P2, uint32_t &R2) {
+  uint32_t r, q0, q1, q2, q3;
   asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
-      ".reg .b32 q0, q1, q2, q3;\n\t.reg .f16 ql, qh, xl, xh;\n\t"
-      "mov.b64 {a0, b0}, %3;\n\tmov.b64 {a1, b1}, %4;\n\tmov.b64 {a2, b2}, %5;\n\tmov.b64 {a3, b3}, %6;\n\t"
+      "mov.b64 {a0, b0}, %5;\n\tmov.b64 {a1, b1}, %6;\n\tmov.b64 {a2, b2}, %7;\n\tmov.b64 {a3, b3}, %8;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
       "mov.b32 %0, {t0, t1, t2, t3};\n\t"
-      "cvt.rn.f16x2.e2m1x2 q0, t0;\n\tcvt.rn.f16x2.e2m1x2 q1, t1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 q2, t2;\n\tcvt.rn.f16x2.e2m1x2 q3, t3;\n\t"
-      "fma.rn.f16x2 %2, q0, q0, %2;\n\tfma.rn.f16x2 %2, q1, q1, %2;\n\t"
-      "fma.rn.f16x2 %2, q2, q2, %2;\n\tfma.rn.f16x2 %2, q3, q3, %2;\n\t"
-      "mov.b32 {ql, qh}, q0;\n\tmov.b32 {xl, xh}, %7;\n\t"
-      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
-      "mov.b32 {ql, qh}, q1;\n\tmov.b32 {xl, xh}, %8;\n\t"
-      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
-      "mov.b32 {ql, qh}, q2;\n\tmov.b32 {xl, xh}, %9;\n\t"
-      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t"
-      "mov.b32 {ql, qh}, q3;\n\tmov.b32 {xl, xh}, %10;\n\t"
-      "fma.rn.f32.f16 %1, ql, xl, %1;\n\tfma.rn.f32.f16 %1, qh, xh, %1;\n\t}"
-      : "=r"(r), "+f"(P), "+r"(R2)
-      : "l"(v0), "l"(v1), "l"(v2), "l"(v3), "r"(h0), "r"(h1), "r"(h2), "r"(h3));
+      "cvt.rn.f16x2.e2m1x2 %1, t0;\n\tcvt.rn.f16x2.e2m1x2 %2, t1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, t2;\n\tcvt.rn.f16x2.e2m1x2 %4, t3;\n\t}"
+      : "=r"(r), "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+      : "l"(v0), "l"(v1), "l"(v2), "l"(v3));
+  const uint32_t q[4] = {q0, q1, q2, q3};
+  const f32x2 x[4] = {x0, x1, x2, x3};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    asm("fma.rn.f16x2 %0, %1, %1, %0;" : "+r"(R2) : "r"(q[k]));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[k]));
+    P2 = fma2(x[k], pack2(f.x, f.y), P2);
+  }
   return r;
 }
 
@@ -216,10 +211,9 @@ __device__ __forceinline__ float f16x2_sum(uint32_t h) {
   return __fadd_rn(f.x, f.y);
 }
 
-// Loads of one block: 2 x 16 bytes -> Block16 (signed fp32 pairs, scaled f16
-// pairs) and the block's max |x| as bf16 bits.  `need_h`: build xh (only the
-// error-comparing rules need P).
-__device__ __forceinline__ uint32_t unpack16(const uint4 &a, const uint4 &b, Block16 &blk, bool need_h) {
+// Loads of one block: 2 x 16 bytes -> Block16 (signed fp32 pairs) and the
+// block's max |x| as bf16 bits.
+__device__ __forceinline__ uint32_t unpack16(const uint4 &a, const uint4 &b, Block16 &blk) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t m = w[0];
 #pragma unroll
@@ -228,23 +222,6 @@ __device__ __forceinline__ uint32_t unpack16(const uint4 &a, const uint4 &b, Blo
   const uint32_t amax_bits = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
   for (int k = 0; k < 8; ++k) blk.x[k] = pack2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-  if (need_h) {
-    // 2^sh with sh = 4 - floor(log2 amax): |x| * 2^sh < 32 for the whole
-    // block, and >= 2^-14 (f16 normal, exact) for every |x| >= amax / 2^18.
-    int e = (int)(amax_bits >> 7);                 // bf16 exponent field
-    int se = min(max(127 + 131 - e, 1), 253);       // biased exponent of 2^sh
-    float sc = __uint_as_float((uint32_t)se << 23);
-    blk.p_unscale = __uint_as_float((uint32_t)(254 - se) << 23);
-    f32x2 sc2 = pack2(sc, sc);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      f32x2 y = mul2(blk.x[k], sc2);
-      float lo, hi;
-      asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y));
-      __half2 hh = __floats2half2_rn(lo, hi);
-      blk.xh[k] = *reinterpret_cast<uint32_t *>(&hh);
-    }
-  }
   return amax_bits;
 }
 
@@ -262,11 +239,13 @@ __device__ __forceinline__ void quant16(const Block16 &blk, float s, float r, ui
 #pragma unroll
   for (int k = 0; k < 8; ++k) w[k] = negdiv2_by_scale(blk.x[k], s2, nr2);
   if (SUMS) {
-    float p = 0.0f;
+    f32x2 p2 = 0ull;  // {+0, +0}
     uint32_t r2h = 0u;
-    c0 = encode8_sums(w[0], w[1], w[2], w[3], blk.xh[0], blk.xh[1], blk.xh[2], blk.xh[3], p, r2h);
-    c1 = encode8_sums(w[4], w[5], w[6], w[7], blk.xh[4], blk.xh[5], blk.xh[6], blk.xh[7], p, r2h);
-    P = __fmul_rn(p, -blk.p_unscale);  // sum of x' * (-q) -> sum |x| q
+    c0 = encode8_sums(w[0], w[1], w[2], w[3], blk.x[0], blk.x[1], blk.x[2], blk.x[3], p2, r2h);
+    c1 = encode8_sums(w[4], w[5], w[6], w[7], blk.x[4], blk.x[5], blk.x[6], blk.x[7], p2, r2h);
+    float plo, phi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(plo), "=f"(phi) : "l"(p2));
+    P = -__fadd_rn(plo, phi);  // sum of x * (-q) -> sum |x| q
     R = f16x2_sum(r2h);
   } else {
     c0 = encode8(w[0], w[1], w[2], w[3]);

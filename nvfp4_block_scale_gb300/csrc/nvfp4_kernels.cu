@@ -78,7 +78,13 @@ __device__ __forceinline__ void block_ff_sum2(FF &a, FF &b, float4 *red) {
 // [SOAR-Q] alpha = max|W| / (6*448), from the per-CTA amax partials.
 __device__ __forceinline__ float fold_alpha(const uint32_t *__restrict__ part, int n, uint32_t *red) {
   uint32_t m = 0;
-  for (int i = threadIdx.x; i < n; i += kThreads) m = max(m, part[i]);
+  for (int i = threadIdx.x; i < n; i += 4 * kThreads) {  // four loads in flight per thread
+    const uint32_t a = part[i];
+    const uint32_t b = i + kThreads < n ? part[i + kThreads] : 0u;
+    const uint32_t c = i + 2 * kThreads < n ? part[i + 2 * kThreads] : 0u;
+    const uint32_t d = i + 3 * kThreads < n ? part[i + 3 * kThreads] : 0u;
+    m = max(max(m, a), max(b, max(c, d)));
+  }
   m = block_max_u32(m, red);
   return __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
 }
@@ -146,8 +152,8 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
 // a2-a4, a7: max rule and FourOverSix
 // ---------------------------------------------------------------------------
 
-// One 16-element block per thread, grid-stride, the next two blocks of the
-// thread in flight while one is computed.  Launched as a programmatic
+// One 16-element block per thread, grid-stride from the last block down, the
+// thread's next two blocks in flight while one is computed.  Launched as a programmatic
 // dependent of k_amax_partials: W was final before that kernel read it, so
 // the first blocks are fetched before the wait.  It lets the next kernel of
 // the stream be scheduled early; that kernel waits for this one to finish.
@@ -161,12 +167,14 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
   __shared__ float s_tab[128], r_tab[128];
   __shared__ uint8_t c4_tab[128];
   constexpr bool FOS = MODE == kModeFourOverSix;
+  // Blocks are walked from the end of the tensor down: the amax pass read the
+  // end last, so for a tensor larger than L2 that part is still cached.
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  int64_t b = B - 1 - ((int64_t)blockIdx.x * kThreads + threadIdx.x);
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
-  const int64_t b1 = b + stride;
-  uint4 n0 = b1 < B ? __ldg(W + 2 * b1) : z, n1 = b1 < B ? __ldg(W + 2 * b1 + 1) : z;
+  uint4 a0 = b >= 0 ? __ldg(W + 2 * b) : z, a1 = b >= 0 ? __ldg(W + 2 * b + 1) : z;
+  const int64_t b1 = b - stride;
+  uint4 n0 = b1 >= 0 ? __ldg(W + 2 * b1) : z, n1 = b1 >= 0 ? __ldg(W + 2 * b1 + 1) : z;
 
   pdl_launch_dependents();
   pdl_wait();
@@ -179,11 +187,11 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
     c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(e4m3_value(threadIdx.x), 1.5f));
   __syncthreads();
 
-  for (; b < B; b += stride) {
-    const int64_t b2 = b + 2 * stride;
-    const uint4 m0 = b2 < B ? __ldg(W + 2 * b2) : z, m1 = b2 < B ? __ldg(W + 2 * b2 + 1) : z;
+  for (; b >= 0; b -= stride) {
+    const int64_t b2 = b - 2 * stride;
+    const uint4 m0 = b2 >= 0 ? __ldg(W + 2 * b2) : z, m1 = b2 >= 0 ? __ldg(W + 2 * b2 + 1) : z;
     Block16 blk;
-    const uint32_t am = unpack16(a0, a1, blk, FOS);
+    const uint32_t am = unpack16(a0, a1, blk);
     const uint32_t d6 = max_rule_code(am, six_a, r6);
     uint32_t c0, c1, d = d6;
     float P6, R6;
