@@ -63,6 +63,8 @@ int device_info(DevInfo **out) {
     if (major != 10 || minor != 3) {
       d.status = NVFP4_ERR_UNSUPPORTED_DEVICE;
     } else {
+      e = prepare_decoupled_kernel();
+      if (e != cudaSuccess) return map_cuda(e);
       for (int k = 0; k < 6; ++k) d.occ[k] = max_active_ctas(k);
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -187,8 +189,9 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int T = cjso ? iters : 0;
   const int g_amax = grid_for(*d, kKernAmax, H / 8 + 1);  // 8 loads per thread per tile
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
-  const int g_cjso = grid_for(*d, kKernCjso, H);
-  const int g_dec = grid_for(*d, kKernDecoupled, B);
+  const int g_cjso = grid_for(*d, kKernCjso, B);
+  const int64_t dec_full = int64_t(d->sms) * d->occ[kKernDecoupled];  // 1024-thread CTAs
+  const int g_dec = (int)((B + 1023) / 1024 < dec_full ? (B + 1023) / 1024 : dec_full);
 
   // scratch: amax partials | 2 x CJSO partial sums | alpha history
   const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);

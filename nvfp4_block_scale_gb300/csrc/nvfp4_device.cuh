@@ -255,6 +255,110 @@ __device__ __forceinline__ void quant16(const Block16 &blk, float s, float r, ui
   c1 ^= 0x88888888u;
 }
 
+// P and R only (no codes): the candidate evaluation of the decoupled search.
+__device__ __forceinline__ void sums8(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, f32x2 x0, f32x2 x1, f32x2 x2,
+                                      f32x2 x3, f32x2 &P2, uint32_t &R2) {
+  uint32_t q0, q1, q2, q3;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+      "mov.b64 {a0, b0}, %4;\n\tmov.b64 {a1, b1}, %5;\n\tmov.b64 {a2, b2}, %6;\n\tmov.b64 {a3, b3}, %7;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, t2;\n\tcvt.rn.f16x2.e2m1x2 %3, t3;\n\t}"
+      : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+      : "l"(v0), "l"(v1), "l"(v2), "l"(v3));
+  const uint32_t q[4] = {q0, q1, q2, q3};
+  const f32x2 x[4] = {x0, x1, x2, x3};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    asm("fma.rn.f16x2 %0, %1, %1, %0;" : "+r"(R2) : "r"(q[k]));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[k]));
+    P2 = fma2(x[k], pack2(f.x, f.y), P2);
+  }
+}
+
+// P = sum |x| q and R = sum q^2 of a block quantized with scale s (no codes).
+__device__ __forceinline__ void block_sums(const Block16 &blk, float s, float r, float &P, float &R) {
+  const f32x2 s2 = pack2(s, s), nr2 = pack2(-r, -r);
+  f32x2 w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) w[k] = negdiv2_by_scale(blk.x[k], s2, nr2);
+  f32x2 p2 = 0ull;
+  uint32_t r2h = 0u;
+  sums8(w[0], w[1], w[2], w[3], blk.x[0], blk.x[1], blk.x[2], blk.x[3], p2, r2h);
+  sums8(w[4], w[5], w[6], w[7], blk.x[4], blk.x[5], blk.x[6], blk.x[7], p2, r2h);
+  float plo, phi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(plo), "=f"(phi) : "l"(p2));
+  P = -__fadd_rn(plo, phi);
+  R = f16x2_sum(r2h);
+}
+
+// The weights of a block as f16 pairs scaled by 2^sh, for the mixed
+// f16 x f16 -> f32 fma of P.  sh = 4 - floor(log2 amax): |x| * 2^sh < 32 for
+// the whole block, and every |x| >= amax / 2^18 -- which includes every
+// element whose code is nonzero for any candidate scale -- has an exact f16
+// image (8 significant bits, f16 normal range).  p_unscale = -2^-sh folds the
+// scale and the sign of the negated quotients back into P.
+struct BlockH16 {
+  uint32_t xh[8];
+  float p_unscale;
+};
+
+__device__ __forceinline__ void make_h16(const Block16 &blk, uint32_t amax_bits, BlockH16 &bh) {
+  const int e = (int)(amax_bits >> 7);            // bf16 exponent field of amax
+  const int se = min(max(258 - e, 1), 253);       // biased exponent of 2^sh
+  const float sc = __uint_as_float((uint32_t)se << 23);
+  bh.p_unscale = -__uint_as_float((uint32_t)(254 - se) << 23);
+  const f32x2 sc2 = pack2(sc, sc);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const f32x2 y = mul2(blk.x[k], sc2);
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y));
+    __half2 hh = __floats2half2_rn(lo, hi);
+    bh.xh[k] = *reinterpret_cast<uint32_t *>(&hh);
+  }
+}
+
+// P (scaled, of the negated codes) and R2 of 4 pairs via mixed fma.
+__device__ __forceinline__ void sums8_h(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, uint32_t h0, uint32_t h1,
+                                        uint32_t h2, uint32_t h3, float &P, uint32_t &R2) {
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+      ".reg .b32 q0, q1, q2, q3;\n\t.reg .f16 ql, qh, xl, xh;\n\t"
+      "mov.b64 {a0, b0}, %2;\n\tmov.b64 {a1, b1}, %3;\n\tmov.b64 {a2, b2}, %4;\n\tmov.b64 {a3, b3}, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
+      "cvt.rn.f16x2.e2m1x2 q0, t0;\n\tcvt.rn.f16x2.e2m1x2 q1, t1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 q2, t2;\n\tcvt.rn.f16x2.e2m1x2 q3, t3;\n\t"
+      "fma.rn.f16x2 %1, q0, q0, %1;\n\tfma.rn.f16x2 %1, q1, q1, %1;\n\t"
+      "fma.rn.f16x2 %1, q2, q2, %1;\n\tfma.rn.f16x2 %1, q3, q3, %1;\n\t"
+      "mov.b32 {ql, qh}, q0;\n\tmov.b32 {xl, xh}, %6;\n\t"
+      "fma.rn.f32.f16 %0, ql, xl, %0;\n\tfma.rn.f32.f16 %0, qh, xh, %0;\n\t"
+      "mov.b32 {ql, qh}, q1;\n\tmov.b32 {xl, xh}, %7;\n\t"
+      "fma.rn.f32.f16 %0, ql, xl, %0;\n\tfma.rn.f32.f16 %0, qh, xh, %0;\n\t"
+      "mov.b32 {ql, qh}, q2;\n\tmov.b32 {xl, xh}, %8;\n\t"
+      "fma.rn.f32.f16 %0, ql, xl, %0;\n\tfma.rn.f32.f16 %0, qh, xh, %0;\n\t"
+      "mov.b32 {ql, qh}, q3;\n\tmov.b32 {xl, xh}, %9;\n\t"
+      "fma.rn.f32.f16 %0, ql, xl, %0;\n\tfma.rn.f32.f16 %0, qh, xh, %0;\n\t}"
+      : "+f"(P), "+r"(R2)
+      : "l"(v0), "l"(v1), "l"(v2), "l"(v3), "r"(h0), "r"(h1), "r"(h2), "r"(h3));
+}
+
+// As block_sums, with P from the block's scaled f16 image.
+__device__ __forceinline__ void block_sums_h(const Block16 &blk, const BlockH16 &bh, float s, float r, float &P,
+                                             float &R) {
+  const f32x2 s2 = pack2(s, s), nr2 = pack2(-r, -r);
+  f32x2 w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) w[k] = negdiv2_by_scale(blk.x[k], s2, nr2);
+  float p = 0.0f;
+  uint32_t r2h = 0u;
+  sums8_h(w[0], w[1], w[2], w[3], bh.xh[0], bh.xh[1], bh.xh[2], bh.xh[3], p, r2h);
+  sums8_h(w[4], w[5], w[6], w[7], bh.xh[4], bh.xh[5], bh.xh[6], bh.xh[7], p, r2h);
+  P = __fmul_rn(p, bh.p_unscale);
+  R = f16x2_sum(r2h);
+}
+
 // Programmatic dependent launch: let the next kernel of the stream be
 // scheduled now / wait until the previous kernel's writes are visible.  Both
 // are no-ops when the launch carries no programmatic dependency.

@@ -23,6 +23,7 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const fl
                     cudaStream_t st);
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
 cudaError_t launch_encode_e4m3(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
+cudaError_t prepare_decoupled_kernel();
 int max_active_ctas(int which);
 
 }  // namespace nvfp4

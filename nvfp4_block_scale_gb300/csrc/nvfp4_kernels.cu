@@ -221,24 +221,42 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
 // a5: CJSO sweeps
 // ---------------------------------------------------------------------------
 
-// One sweep.  INIT: max rule from the amax partials.  Otherwise: alpha from
-// the previous sweep's partial sums ([SOAR-A]), re-quantize with the stored
-// Delta, Delta* ([SOAR-D]) rounded to E4M3, re-quantize ([SOAR-SCHED]).
-// Every sweep stores Delta, writes the partial sums sum Delta*P and
-// sum Delta^2*R of its CTA, and records alpha in alpha_hist[t].
+// One sweep over all blocks, one block per thread.  INIT: max rule from the
+// amax partials.  Otherwise: alpha from the previous sweep's partial sums
+// ([SOAR-A]), sums with the stored Delta, Delta* ([SOAR-D]) rounded to E4M3,
+// re-quantize ([SOAR-SCHED]).  Every sweep stores Delta, writes its CTA's
+// partial sums sum Delta*P and sum Delta^2*R, and records alpha in
+// alpha_hist[t].  Sweeps chain by programmatic dependent launch: each prefetches
+// its first blocks of W (an input, final before the chain began) and then
+// waits for the previous sweep before reading the partials and the scales.
+// `descending` alternates between sweeps so that each starts on the part of
+// W the previous one read last (still in L2 when W is larger than L2).
 template <bool INIT>
-__global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict__ W, int64_t H,
+__global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict__ W, int64_t B,
                                                          const uint32_t *__restrict__ amax_part, int n_amax,
                                                          const float4 *__restrict__ part_in, int n_in,
                                                          float4 *__restrict__ part_out,
                                                          float *__restrict__ alpha_hist, int t,
                                                          uint8_t *__restrict__ scales,
                                                          uint32_t *__restrict__ codes32, int write_codes,
-                                                         float *__restrict__ alpha_out, int write_alpha) {
+                                                         float *__restrict__ alpha_out, int write_alpha,
+                                                         int descending) {
   __shared__ uint32_t red[kWarps];
   __shared__ float4 redf[kWarps];
-  __shared__ float s_tab[128], r_tab[128];
+  __shared__ float s_tab[128], r_tab[128], ev_tab[128];
   __shared__ float sh_alpha;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t step = descending ? -stride : stride;
+  int64_t b = descending ? B - 1 - i0 : i0;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  auto ok = [&](int64_t x) { return x >= 0 && x < B; };
+  uint4 a0 = ok(b) ? __ldg(W + 2 * b) : z, a1 = ok(b) ? __ldg(W + 2 * b + 1) : z;
+  uint4 n0 = ok(b + step) ? __ldg(W + 2 * (b + step)) : z, n1 = ok(b + step) ? __ldg(W + 2 * (b + step) + 1) : z;
+  if (threadIdx.x < 128) ev_tab[threadIdx.x] = e4m3_value(threadIdx.x);
+
+  pdl_launch_dependents();
+  pdl_wait();
   float alpha;
   if (INIT) {
     alpha = fold_alpha(amax_part, n_amax, red);
@@ -268,105 +286,125 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   __syncthreads();
 
   FF num = {0.0f, 0.0f}, den = {0.0f, 0.0f};
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t base = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 32; base < H;
-       base += nwarps * 32) {
-    const int64_t h = base + lane;
-    const bool valid = h < H;
-    float ax[8];
-    uint32_t sgn, am;
-    unpack8(load_half(W, h, valid), ax, sgn, am);
+  for (; ok(b); b += step) {
+    const int64_t b2 = b + 2 * step;
+    const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
+    Block16 blk;
+    const uint32_t am = unpack16(a0, a1, blk);
     uint32_t d;
-    HalfQ q;
     float P, R;
     if (INIT) {
-      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
       d = max_rule_code(am, six_a, r6);
-      q = quant_half(ax, s_tab[d], r_tab[d]);
     } else {
-      d = valid ? scales[h >> 1] : 0u;
-      q = quant_half(ax, s_tab[d], r_tab[d]);
-      P = __fadd_rn(q.P, __shfl_xor_sync(0xFFFFFFFFu, q.P, 1));
-      R = __fadd_rn(q.R, __shfl_xor_sync(0xFFFFFFFFu, q.R, 1));
+      d = scales[b];
+      block_sums(blk, s_tab[d], r_tab[d], P, R);
       if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
-      q = quant_half(ax, s_tab[d], r_tab[d]);
     }
-    P = __fadd_rn(q.P, __shfl_xor_sync(0xFFFFFFFFu, q.P, 1));
-    R = __fadd_rn(q.R, __shfl_xor_sync(0xFFFFFFFFu, q.R, 1));
-    if (valid) {
-      if (write_codes) codes32[h] = q.mags | sgn;
-      if (!(lane & 1)) {
-        scales[h >> 1] = (uint8_t)d;
-        const float dv = e4m3_value(d);
-        ff_add_prod(num, dv, P);                    // exact product, compensated sum
-        ff_add(den, __fmul_rn(__fmul_rn(dv, dv), R), 0.0f);  // Delta^2 * R is exact in fp32
-      }
+    if (write_codes) {
+      uint32_t c0, c1;
+      quant16<true>(blk, s_tab[d], r_tab[d], c0, c1, P, R);
+      codes32[2 * b] = c0;
+      codes32[2 * b + 1] = c1;
+    } else {
+      block_sums(blk, s_tab[d], r_tab[d], P, R);
     }
+    scales[b] = (uint8_t)d;
+    const float dv = ev_tab[d];
+    ff_add_prod(num, dv, P);                             // exact product, compensated sum
+    ff_add(den, __fmul_rn(__fmul_rn(dv, dv), R), 0.0f);  // Delta^2 * R is exact in fp32
+    a0 = n0;
+    a1 = n1;
+    n0 = m0;
+    n1 = m1;
   }
   block_ff_sum2(num, den, redf);
   if (threadIdx.x == 0) part_out[blockIdx.x] = make_float4(num.hi, num.lo, den.hi, den.lo);
 }
 
 // ---------------------------------------------------------------------------
-// a6: decoupled search (one thread per block, block held in registers)
+// a6: decoupled search
 // ---------------------------------------------------------------------------
+//
+// Every candidate constant depends only on (Delta^d0 code, k): the quotient
+// scale sq = fl(alpha * fl(Delta^d0 * m_k)), its reciprocal, and the dequant
+// scales fl(alpha * Delta^d) of the two E4M3 values bracketing Delta^q.  Each
+// CTA tabulates them for all 128 codes x 101 multipliers in shared memory
+// (206,848 bytes), so the search over a block reads one float4 per candidate.
+// One block per thread, held in registers.  [SOAR-DEC]
+constexpr int kDecThreads = 1024;
+constexpr int kDecK = 101;
+constexpr size_t kDecTableBytes = (size_t)128 * kDecK * sizeof(float4);
 
-__global__ void __launch_bounds__(kThreads) k_decoupled(const uint4 *__restrict__ W, int64_t B,
-                                                        const float *__restrict__ alpha_hist, int t,
-                                                        uint8_t *__restrict__ scales,
-                                                        uint32_t *__restrict__ codes32) {
-  __shared__ float ev_tab[128], sd_tab[128], m_tab[101];
-  const float alpha = alpha_hist[t];
-  if (threadIdx.x < 128) {
-    const float ev = e4m3_value(threadIdx.x);
-    ev_tab[threadIdx.x] = ev;
-    sd_tab[threadIdx.x] = __fmul_rn(alpha, ev);
-  }
-  if (threadIdx.x < 101)  // [SOAR-DEC] multipliers 0.50, 0.51, ..., 1.50 rounded to fp32
+__device__ __forceinline__ void bracket_e4m3(float dq, const float *ev_tab, uint32_t &lo, uint32_t &hi) {
+  const uint32_t n = e4m3_code(dq);  // the two E4M3 values around dq (448 above 448)
+  const float vn = ev_tab[n];
+  lo = vn > dq ? n - 1u : n;
+  hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
+                                                              const float *__restrict__ alpha_hist, int t,
+                                                              uint8_t *__restrict__ scales,
+                                                              uint32_t *__restrict__ codes32) {
+  extern __shared__ float4 tab[];  // [code][k] = {sq, rq, sd_lo, sd_hi}
+  __shared__ float ev_tab[128], m_tab[kDecK];
+  const int64_t stride = (int64_t)gridDim.x * kDecThreads;
+  int64_t b = (int64_t)blockIdx.x * kDecThreads + threadIdx.x;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
+  if (threadIdx.x < 128) ev_tab[threadIdx.x] = e4m3_value(threadIdx.x);
+  if (threadIdx.x < kDecK)  // m_k = fl32((50 + k) / 100)
     m_tab[threadIdx.x] = __double2float_rn(__ddiv_rn((double)(50 + threadIdx.x), 100.0));
+  pdl_launch_dependents();
+  pdl_wait();
+  const float alpha = alpha_hist[t];
+  __syncthreads();
+  for (int e = threadIdx.x; e < 128 * kDecK; e += kDecThreads) {
+    const int c = e / kDecK, k = e - c * kDecK;
+    const float dq = __fmul_rn(ev_tab[c], m_tab[k]);
+    const float sq = __fmul_rn(alpha, dq);
+    uint32_t lo, hi;
+    bracket_e4m3(dq, ev_tab, lo, hi);
+    tab[e] = make_float4(sq, sq > 0.0f ? __frcp_rn(sq) : 0.0f, __fmul_rn(alpha, ev_tab[lo]),
+                         __fmul_rn(alpha, ev_tab[hi]));
+  }
   __syncthreads();
 
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < B; b += (int64_t)gridDim.x * kThreads) {
-    float ax0[8], ax1[8];
-    uint32_t sg0, sg1, am;
-    unpack8(__ldg(W + 2 * b), ax0, sg0, am);
-    unpack8(__ldg(W + 2 * b + 1), ax1, sg1, am);
+  for (; b < B; b += stride) {
+    const int64_t nb = b + stride;
+    const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
+    Block16 blk;
+    const uint32_t am = unpack16(a0, a1, blk);
     const uint32_t d0 = scales[b];
-    const float delta0 = ev_tab[d0];
-    uint32_t best_d = d0, best_k = 0;
-    bool any = __fmul_rn(alpha, delta0) != 0.0f;
-    if (any) {
+    uint32_t best_d = d0, c0, c1;
+    float P, R;
+    if (__fmul_rn(alpha, ev_tab[d0]) != 0.0f) {
+      BlockH16 bh;
+      make_h16(blk, am, bh);
+      const float4 *row = tab + d0 * kDecK;
       float best_g = __int_as_float(0x7F800000);  // +inf
-      for (int k = 0; k <= 100; ++k) {
-        const float dq = __fmul_rn(delta0, m_tab[k]);
-        const float sq = __fmul_rn(alpha, dq);
-        const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
-        HalfQ a = quant_half(ax0, sq, rq);
-        HalfQ c = quant_half(ax1, sq, rq);
-        const float P = __fadd_rn(a.P, c.P), R = __fadd_rn(a.R, c.R);
-        // the two E4M3 values bracketing dq (448 above 448)
-        const uint32_t n = e4m3_code(dq);
-        const float vn = ev_tab[n];
-        const uint32_t lo = vn > dq ? n - 1u : n;
-        const uint32_t hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
-        const float glo = cand_err(sd_tab[lo], P, R);
-        const float ghi = cand_err(sd_tab[hi], P, R);
-        if (glo < best_g) { best_g = glo; best_d = lo; best_k = k; }
-        if (ghi < best_g) { best_g = ghi; best_d = hi; best_k = k; }
+      int best_k = 0, best_h = 0;
+      for (int k = 0; k < kDecK; ++k) {
+        const float4 c = row[k];
+        block_sums_h(blk, bh, c.x, c.y, P, R);
+        const float glo = cand_err(c.z, P, R);
+        const float ghi = cand_err(c.w, P, R);
+        if (glo < best_g) { best_g = glo; best_k = k; best_h = 0; }
+        if (ghi < best_g) { best_g = ghi; best_k = k; best_h = 1; }
       }
+      const float4 c = row[best_k];
+      quant16<false>(blk, c.x, c.y, c0, c1, P, R);
+      uint32_t lo, hi;
+      bracket_e4m3(__fmul_rn(ev_tab[d0], m_tab[best_k]), ev_tab, lo, hi);
+      best_d = best_h ? hi : lo;
+    } else {
+      quant16<false>(blk, 0.0f, 0.0f, c0, c1, P, R);  // zero scale: sign-only codes
     }
-    uint32_t m0 = 0, m1 = 0;
-    if (any) {
-      const float dq = __fmul_rn(delta0, m_tab[best_k]);
-      const float sq = __fmul_rn(alpha, dq);
-      const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
-      m0 = quant_half(ax0, sq, rq).mags;
-      m1 = quant_half(ax1, sq, rq).mags;
-    }
-    codes32[2 * b] = m0 | sg0;  // two 4-byte stores: codes is only 4-byte aligned
-    codes32[2 * b + 1] = m1 | sg1;
+    codes32[2 * b] = c0;
+    codes32[2 * b + 1] = c1;
     scales[b] = (uint8_t)best_d;
+    a0 = n0;
+    a1 = n1;
   }
 }
 
@@ -463,20 +501,38 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
                               uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                               int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const uint4 *w = static_cast<const uint4 *>(W);
   uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  const int64_t B = H / 2;
+  const int descending = (t & 1) == 0;  // amax reads ascending; sweeps alternate from there
   if (init)
-    return cudaLaunchKernelEx(&cfg, k_cjso_sweep<true>, w, H, amax_part, n_amax, part_in, n_in, part_out,
-                              alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha);
-  return cudaLaunchKernelEx(&cfg, k_cjso_sweep<false>, w, H, amax_part, n_amax, part_in, n_in, part_out,
-                            alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha);
+    return cudaLaunchKernelEx(&cfg, k_cjso_sweep<true>, w, B, amax_part, n_amax, part_in, n_in, part_out,
+                              alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha, descending);
+  return cudaLaunchKernelEx(&cfg, k_cjso_sweep<false>, w, B, amax_part, n_amax, part_in, n_in, part_out,
+                            alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha, descending);
 }
 
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
                              uint8_t *codes, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecTableBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_decoupled, static_cast<const uint4 *>(W), B, alpha_hist, t, scales,
                             reinterpret_cast<uint32_t *>(codes));
+}
+
+cudaError_t prepare_decoupled_kernel() {
+  return cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
 }
 
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out,
@@ -504,7 +560,9 @@ int max_active_ctas(int which) {
     case kKernQuantMax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeMax>, kThreads, 0); break;
     case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
     case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
-    case kKernDecoupled: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kThreads, 0); break;
+    case kKernDecoupled:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kDecThreads, kDecTableBytes);
+      break;
     default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_dequant, kThreads, 0); break;
   }
   return (e == cudaSuccess && n > 0) ? n : 1;
