@@ -297,18 +297,17 @@ __device__ __forceinline__ void block_sums(const Block16 &blk, float s, float r,
 // f16 x f16 -> f32 fma of P.  sh = 4 - floor(log2 amax): |x| * 2^sh < 32 for
 // the whole block, and every |x| >= amax / 2^18 -- which includes every
 // element whose code is nonzero for any candidate scale -- has an exact f16
-// image (8 significant bits, f16 normal range).  p_unscale = -2^-sh folds the
-// scale and the sign of the negated quotients back into P.
+// image (8 significant bits, f16 normal range).
 struct BlockH16 {
   uint32_t xh[8];
-  float p_unscale;
+  float m2_unscale;  // 2 * 2^-sh: P = -(scaled sum) * 2^-sh, so -2P = scaled sum * m2_unscale
 };
 
 __device__ __forceinline__ void make_h16(const Block16 &blk, uint32_t amax_bits, BlockH16 &bh) {
   const int e = (int)(amax_bits >> 7);            // bf16 exponent field of amax
   const int se = min(max(258 - e, 1), 253);       // biased exponent of 2^sh
   const float sc = __uint_as_float((uint32_t)se << 23);
-  bh.p_unscale = -__uint_as_float((uint32_t)(254 - se) << 23);
+  bh.m2_unscale = __uint_as_float((uint32_t)(255 - se) << 23);  // 2^(1 - sh)
   const f32x2 sc2 = pack2(sc, sc);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -344,9 +343,10 @@ __device__ __forceinline__ void sums8_h(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, 
       : "l"(v0), "l"(v1), "l"(v2), "l"(v3), "r"(h0), "r"(h1), "r"(h2), "r"(h3));
 }
 
-// As block_sums, with P from the block's scaled f16 image.
-__device__ __forceinline__ void block_sums_h(const Block16 &blk, const BlockH16 &bh, float s, float r, float &P,
-                                             float &R) {
+// As block_sums, with P from the block's scaled f16 image; returns -2P (one
+// exact power-of-two multiply of the scaled sum) for the error comparisons.
+__device__ __forceinline__ void block_sums_h(const Block16 &blk, const BlockH16 &bh, float s, float r,
+                                             float &m2P, float &R) {
   const f32x2 s2 = pack2(s, s), nr2 = pack2(-r, -r);
   f32x2 w[8];
 #pragma unroll
@@ -355,8 +355,13 @@ __device__ __forceinline__ void block_sums_h(const Block16 &blk, const BlockH16 
   uint32_t r2h = 0u;
   sums8_h(w[0], w[1], w[2], w[3], bh.xh[0], bh.xh[1], bh.xh[2], bh.xh[3], p, r2h);
   sums8_h(w[4], w[5], w[6], w[7], bh.xh[4], bh.xh[5], bh.xh[6], bh.xh[7], p, r2h);
-  P = __fmul_rn(p, bh.p_unscale);
+  m2P = __fmul_rn(p, bh.m2_unscale);
   R = f16x2_sum(r2h);
+}
+
+// cand_err with -2P given: s * (s*R - 2P).
+__device__ __forceinline__ float cand_err_m2p(float s, float m2P, float R) {
+  return __fmul_rn(s, __fmaf_rn(s, R, m2P));
 }
 
 // Programmatic dependent launch: let the next kernel of the stream be

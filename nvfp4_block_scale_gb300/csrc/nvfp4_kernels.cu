@@ -386,9 +386,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
       int best_k = 0, best_h = 0;
       for (int k = 0; k < kDecK; ++k) {
         const float4 c = row[k];
-        block_sums_h(blk, bh, c.x, c.y, P, R);
-        const float glo = cand_err(c.z, P, R);
-        const float ghi = cand_err(c.w, P, R);
+        float m2P;
+        block_sums_h(blk, bh, c.x, c.y, m2P, R);
+        const float glo = cand_err_m2p(c.z, m2P, R);
+        const float ghi = cand_err_m2p(c.w, m2P, R);
         if (glo < best_g) { best_g = glo; best_k = k; best_h = 0; }
         if (ghi < best_g) { best_g = ghi; best_k = k; best_h = 1; }
       }
