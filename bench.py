@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
 HEADLINE = "studentt_4k"
-MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3}
+MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4}
 
 
 def _synth():
@@ -55,13 +55,14 @@ WORKLOADS = {
                     "4096x4096 bf16, Student-t df=4 std 0.02, 0.1% columns x20 (seed 1 + rank)",
                     ("max", "four_over_six")),
     "gauss_1k": (lambda r: _synth().gauss_1k(seed=0 + r),
-                 "1024x1024 bf16, N(0,0.02) (seed 0 + rank)", ("max", "four_over_six", "cjso", "cjso_decoupled")),
+                 "1024x1024 bf16, N(0,0.02) (seed 0 + rank)",
+                 ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")),
     "mlp_up": (lambda r: _synth().mlp_up(seed=2 + r),
                "4096x14336 bf16, 10% rows N(0,0.05), rest N(0,0.015) (seed 2 + rank)",
                ("max", "four_over_six", "cjso", "cjso_decoupled")),
     "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
                 "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)",
-                ("max", "four_over_six", "cjso", "cjso_decoupled")),
+                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")),
 }
 
 ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
@@ -70,7 +71,7 @@ DECOUPLED_FLOPS = 101 * 9  # per element: 101 candidates x (quotient 5 + P, R 4)
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters}[mode]
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1}[mode]
 
 
 def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
@@ -79,6 +80,8 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
     if mode in (0, 1):
         b = ONE_PASS if fits else TWO_PASS
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W <= L2/2: one HBM read' if fits else 'W read twice'})"
+    if mode == 4:  # dequantize: codes + scales in, bf16 out
+        return "hbm", "GB/s", ONE_PASS * n, "2.5625 B/elem (codes 0.5 + scales 1/16 read, bf16 2 written)"
     if mode == 2:
         b = ONE_PASS if fits else (iters + 2) * 2 + 0.5625
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W stays in L2' if fits else f'{iters + 2} reads of W'})"
@@ -238,14 +241,27 @@ def run_ours(args, modes):
     mids = [MODE_IDS[m] for m in modes]
     outs = {m: (torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
-                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids}
+                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids if m != 4}
+
+    if 4 in mids:  # dequantize inputs: this tensor quantized (max rule) once per rotation slot
+        dq_in = []
+        for i in range(ncopy):
+            c, sc, a = nv.quantize(Wd[i], nv.MAX)
+            dq_in.append((c, sc, a))
+        dq_out = [torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) for _ in range(ncopy)]
 
     def call(mode, w, s):
-        c, sc, a = outs[mode]
-        st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
-                               a.data_ptr(), s.cuda_stream)
+        if mode == 4:  # dequantize the slot of this W into that slot's output
+            i = next(k for k in range(ncopy) if Wd[k] is w)
+            c, sc, a = dq_in[i]
+            st = nv.nvfp4_dequantize(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, dq_out[i].data_ptr(),
+                                     s.cuda_stream)
+        else:
+            c, sc, a = outs[mode]
+            st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
+                                   a.data_ptr(), s.cuda_stream)
         if st != 0:
-            raise RuntimeError(f"nvfp4_quantize: {nv.nvfp4_status_string(st)}")
+            raise RuntimeError(f"nvfp4 call: {nv.nvfp4_status_string(st)}")
 
     def step(i, s):
         for j, m in enumerate(mids):
@@ -384,11 +400,12 @@ def run_ours(args, modes):
     # ---- end to end through the C ABI with pinned host buffers
     W_pin = W_host.pin_memory()
     Wd0 = torch.empty_like(Wd[0])
-    host_outs = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m]) for m in mids}
+    qmids = [m for m in mids if m != 4]
+    host_outs = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m]) for m in qmids}
 
     def e2e_step():
         Wd0.copy_(W_pin, non_blocking=True)
-        for m in mids:
+        for m in qmids:
             call(m, Wd0, stream)
             for dst, src in zip(host_outs[m], outs[m]):
                 dst.copy_(src, non_blocking=True)
@@ -410,12 +427,14 @@ def run_ours(args, modes):
     if ws > 1:
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     d2h = sum(t.numel() * t.element_size() for m in host_outs for t in host_outs[m])
-    out["e2e"] = {"value": ws * bytes_per_step * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
+    out["e2e"] = {"value": ws * len(qmids) * 2 * n * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
+                  "modes": [m for m in modes if m != "dequant"],
                   "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e}
 
     if rank == 0 and ws == 1:
         rows_cap = None if n <= (1 << 24) else max(16, (1 << 22) // cols)
-        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, modes, args.iters, max_rows=rows_cap)
+        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, [m for m in modes if m != "dequant"], args.iters,
+                                                  max_rows=rows_cap)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -435,8 +454,10 @@ def run_reference(args, modes):
     sample = w_bits[:rows]  # bounded per-step sample of the workload
     threads = os.cpu_count() or 1
 
+    qmodes = [m for m in modes if m != "dequant"]
+
     def step():
-        for m in modes:
+        for m in qmodes:
             oracle.quantize(sample, MODE_IDS[m], args.iters, threads=threads)
 
     for _ in range(max(args.warmup, 3)):
@@ -445,7 +466,7 @@ def run_reference(args, modes):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = len(modes) * sample.nbytes * args.steps / el / 1e9
+    value = len(qmodes) * sample.nbytes * args.steps / el / 1e9
     sdesc = (f"C oracle, {threads} host threads, rows 0..{rows - 1} of the {w_bits.shape[0]}x{w_bits.shape[1]} "
              f"tensor per step, {'+'.join(modes)}")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,

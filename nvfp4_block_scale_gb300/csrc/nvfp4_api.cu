@@ -31,6 +31,7 @@ struct DevInfo {
   bool ready = false;
   int status = NVFP4_OK;
   int sms = 0;
+  int l2 = 0;  // L2 bytes
   int occ[6] = {1, 1, 1, 1, 1, 1};
   cudaMemPool_t pool = nullptr;
 };
@@ -59,6 +60,7 @@ int device_info(DevInfo **out) {
     e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.l2, cudaDevAttrL2CacheSize, dev);
     if (e != cudaSuccess) return map_cuda(e);
     if (major != 10 || minor != 3) {
       d.status = NVFP4_ERR_UNSUPPORTED_DEVICE;
@@ -187,7 +189,8 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int64_t H = n / 8;   // half blocks = 16-byte loads
   const int64_t B = n / 16;  // blocks
   const int T = cjso ? iters : 0;
-  const int g_amax = grid_for(*d, kKernAmax, H / 8 + 1);  // 8 loads per thread per tile
+  const int g_amax = grid_for(*d, kKernAmax, H / 16 + 1);  // 16 loads per thread per tile
+  const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
   const int64_t dec_full = int64_t(d->sms) * d->occ[kKernDecoupled];  // 1024-thread CTAs
@@ -212,7 +215,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   }
   if (e == cudaSuccess && !cjso) {
     TraceScope tr(mode == kModeFourOverSix ? kTrQuantFos : kTrQuantMax, stream);
-    e = launch_quant_max_fos(mode, W, H, amax_part, g_amax, codes, scales, alpha, g_quant, stream);
+    e = launch_quant_max_fos(mode, W, H, amax_part, g_amax, codes, scales, alpha, g_quant, ranged, stream);
   } else if (e == cudaSuccess) {
     const bool plain = mode == kModeCjso;
     {

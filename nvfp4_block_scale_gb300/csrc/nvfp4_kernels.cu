@@ -119,15 +119,15 @@ __device__ __forceinline__ uint4 load_half(const uint4 *__restrict__ W, int64_t 
 // the stream, it waits for that grid before touching W, then lets the
 // quantize kernel be scheduled at once; that kernel waits for this grid's
 // completion before reading the partials.
-constexpr int kAmaxUnroll = 8;
+constexpr int kAmaxUnroll = 16;
 
 __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restrict__ W, int64_t n16,
                                                             uint32_t *__restrict__ part) {
   __shared__ uint32_t red[kWarps];
+  const int64_t tile = (int64_t)kThreads * kAmaxUnroll;
   pdl_wait();  // W may be written by the previous kernel of the stream
   pdl_launch_dependents();
   uint32_t m = 0u;
-  const int64_t tile = (int64_t)kThreads * kAmaxUnroll;
   for (int64_t base = (int64_t)blockIdx.x * tile + threadIdx.x; base < n16; base += (int64_t)gridDim.x * tile) {
     uint4 v[kAmaxUnroll];
 #pragma unroll
@@ -152,44 +152,62 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
 // a2-a4, a7: max rule and FourOverSix
 // ---------------------------------------------------------------------------
 
-// One 16-element block per thread, grid-stride from the last block down, the
-// thread's next two blocks in flight while one is computed.  Launched as a programmatic
-// dependent of k_amax_partials: W was final before that kernel read it, so
-// the first blocks are fetched before the wait.  It lets the next kernel of
-// the stream be scheduled early; that kernel waits for this one to finish.
+// One 16-element block per thread, the thread's next two blocks in flight
+// while one is computed.  Two block orders: `ranged` (W fits in L2, so the
+// order does not matter for traffic) gives every CTA a contiguous, equal
+// range, so all SMs finish together; otherwise the grid strides from the last
+// block down, because the amax pass read the end of W last and that part is
+// still in L2.  Launched as a programmatic dependent of k_amax_partials: W was
+// final before that kernel read it, so the first blocks are fetched before the
+// wait.  It lets the next kernel of the stream be scheduled early; that kernel
+// waits for this one to finish.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restrict__ W, int64_t B,
                                                             const uint32_t *__restrict__ amax_part, int n_amax,
                                                             uint32_t *__restrict__ codes32,
                                                             uint8_t *__restrict__ scales,
-                                                            float *__restrict__ alpha_out) {
+                                                            float *__restrict__ alpha_out, int ranged) {
   __shared__ uint32_t red[kWarps];
-  __shared__ float s_tab[128], r_tab[128];
+  __shared__ float s_tab[128], r_tab[128], ev_tab[128];
   __shared__ uint8_t c4_tab[128];
   constexpr bool FOS = MODE == kModeFourOverSix;
-  // Blocks are walked from the end of the tensor down: the amax pass read the
-  // end last, so for a tensor larger than L2 that part is still cached.
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
-  int64_t b = B - 1 - ((int64_t)blockIdx.x * kThreads + threadIdx.x);
+  int64_t b, step, end;
+  if (ranged) {  // blocks [B*c/G, B*(c+1)/G) of CTA c, ascending
+    b = B * blockIdx.x / gridDim.x + threadIdx.x;
+    end = B * (blockIdx.x + 1) / gridDim.x;
+    step = kThreads;
+  } else {  // grid-stride from the last block down
+    b = B - 1 - ((int64_t)blockIdx.x * kThreads + threadIdx.x);
+    step = -(int64_t)gridDim.x * kThreads;
+    end = -1;
+  }
+  auto ok = [&](int64_t x) { return ranged ? x < end : x > end; };
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  uint4 a0 = b >= 0 ? __ldg(W + 2 * b) : z, a1 = b >= 0 ? __ldg(W + 2 * b + 1) : z;
-  const int64_t b1 = b - stride;
-  uint4 n0 = b1 >= 0 ? __ldg(W + 2 * b1) : z, n1 = b1 >= 0 ? __ldg(W + 2 * b1 + 1) : z;
+  uint4 a0 = ok(b) ? __ldg(W + 2 * b) : z, a1 = ok(b) ? __ldg(W + 2 * b + 1) : z;
+  const int64_t b1 = b + step;
+  uint4 n0 = ok(b1) ? __ldg(W + 2 * b1) : z, n1 = ok(b1) ? __ldg(W + 2 * b1 + 1) : z;
+  if (threadIdx.x < 128) {  // alpha-independent part of the tables
+    const float ev = e4m3_value(threadIdx.x);
+    ev_tab[threadIdx.x] = ev;
+    if (FOS) c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(ev, 1.5f));  // [FOS-02] scale_m4 = fp8(scale_m6 * 1.5)
+  }
 
   pdl_launch_dependents();
   pdl_wait();
-  const float alpha = fold_alpha(amax_part, n_amax, red);
+  const float alpha = fold_alpha(amax_part, n_amax, red);  // (its barriers also publish ev_tab)
   if (blockIdx.x == 0 && threadIdx.x == 0) *alpha_out = alpha;
   const float six_a = __fmul_rn(alpha, 6.0f);
   const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
-  build_scale_tables(alpha, s_tab, r_tab);
-  if (FOS && threadIdx.x < 128)  // [FOS-02] scale_m4 = fp8(scale_m6 * 1.5)
-    c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(e4m3_value(threadIdx.x), 1.5f));
+  if (threadIdx.x < 128) {
+    const float sv = __fmul_rn(alpha, ev_tab[threadIdx.x]);
+    s_tab[threadIdx.x] = sv;
+    r_tab[threadIdx.x] = sv > 0.0f ? __frcp_rn(sv) : 0.0f;
+  }
   __syncthreads();
 
-  for (; b >= 0; b -= stride) {
-    const int64_t b2 = b - 2 * stride;
-    const uint4 m0 = b2 >= 0 ? __ldg(W + 2 * b2) : z, m1 = b2 >= 0 ? __ldg(W + 2 * b2 + 1) : z;
+  for (; ok(b); b += step) {
+    const int64_t b2 = b + 2 * step;
+    const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
     const uint32_t d6 = max_rule_code(am, six_a, r6);
@@ -482,7 +500,8 @@ cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int
 }
 
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
-                                 uint8_t *codes, uint8_t *scales, float *alpha, int grid, cudaStream_t st) {
+                                 uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
+                                 cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -493,8 +512,9 @@ cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint3
   uint32_t *c = reinterpret_cast<uint32_t *>(codes);
   const int64_t B = H / 2;
   if (mode == kModeFourOverSix)
-    return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeFourOverSix>, w, B, amax_part, n_amax, c, scales, alpha);
-  return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, B, amax_part, n_amax, c, scales, alpha);
+    return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeFourOverSix>, w, B, amax_part, n_amax, c, scales, alpha,
+                              ranged);
+  return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, B, amax_part, n_amax, c, scales, alpha, ranged);
 }
 
 cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,

@@ -43,6 +43,7 @@ struct NoAllocDev {
   bool ready = false;
   int status = NVFP4_OK;
   int sms = 0;
+  int l2 = 0;
   int occ_max = 1, occ_fos = 1;
   uint32_t *scratch = nullptr;  // device address of g_noalloc_scratch
 };
@@ -70,6 +71,7 @@ int na_device(NoAllocDev **out) {
     e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.l2, cudaDevAttrL2CacheSize, dev);
     if (e != cudaSuccess) return na_map(e);
     if (major != 10 || minor != 3) {
       d.status = NVFP4_ERR_UNSUPPORTED_DEVICE;
@@ -121,6 +123,8 @@ extern "C" int nvfp4_quantize_noalloc(const void *W, int64_t rows, int64_t cols,
   if (g_amax > kNoAllocMaxCtas) return NVFP4_ERR_INVALID_ARG;
   const int g_quant = na_grid(d->sms, mode == kModeFourOverSix ? d->occ_fos : d->occ_max, n / 16);
   cudaError_t e = launch_amax_partials(W, H, d->scratch, g_amax, stream);
-  if (e == cudaSuccess) e = launch_quant_max_fos(mode, W, H, d->scratch, g_amax, codes, scales, alpha, g_quant, stream);
+  const int ranged = 2 * n <= int64_t(d->l2) / 2;
+  if (e == cudaSuccess)
+    e = launch_quant_max_fos(mode, W, H, d->scratch, g_amax, codes, scales, alpha, g_quant, ranged, stream);
   return na_map(e);
 }

@@ -28,58 +28,72 @@ MAX, FOUR_OVER_SIX, CJSO, CJSO_DECOUPLED = 0, 1, 2, 3
 MODE_NAMES = {MAX: "max", FOUR_OVER_SIX: "four_over_six", CJSO: "cjso", CJSO_DECOUPLED: "cjso_decoupled"}
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compiles an oracle C source into shared library `out` with gcc (no
+    fused multiply-add contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fno-fast-math",
+           "-Wall", "-shared", "-fPIC", "-o", tmp, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compiles the oracle with gcc (no fused multiply-add contraction)."""
+    """Compiles the oracle (once; again when the source is newer)."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(LIB_PATH)
             and os.path.getmtime(LIB_PATH) >= os.path.getmtime(SRC)):
         return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-ffp-contract=off", "-fno-fast-math",
-           "-Wall", "-shared", "-fPIC", "-o", tmp, SRC, "-lm", "-lpthread"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    return compile_source(SRC, LIB_PATH)
 
 
 _lib = None
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads an oracle shared library and declares its functions."""
+    L = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    ci = ctypes.c_int
+    L.oracle_quantize.argtypes = [p, i64, i64, ci, ci, p, p, p, p, ci]
+    L.oracle_quantize.restype = ci
+    L.oracle_quantize_sampled.argtypes = [p, i64, i64, ci, ci, p, i64, p, p, p, ci]
+    L.oracle_quantize_sampled.restype = ci
+    L.oracle_dequantize.argtypes = [p, p, ctypes.c_float, i64, i64, p]
+    L.oracle_dequantize.restype = ci
+    L.oracle_mse.argtypes = [p, p, p, ctypes.c_float, i64]
+    L.oracle_mse.restype = ctypes.c_double
+    L.oracle_block_sse.argtypes = [p, p, p, ctypes.c_float, i64, p]
+    L.oracle_block_sse.restype = None
+    L.oracle_cjso_trace.argtypes = [p, i64, i64, ci, p, p]
+    L.oracle_cjso_trace.restype = ci
+    L.oracle_e2m1_encode.argtypes = [p, i64, p]
+    L.oracle_e2m1_encode.restype = None
+    L.oracle_e4m3_encode.argtypes = [p, i64, p]
+    L.oracle_e4m3_encode.restype = None
+    L.oracle_e4m3_floor_ceil.argtypes = [p, i64, p, p]
+    L.oracle_e4m3_floor_ceil.restype = None
+    L.oracle_e2m1_value.argtypes = [ci]
+    L.oracle_e2m1_value.restype = ctypes.c_double
+    L.oracle_e4m3_value.argtypes = [ci]
+    L.oracle_e4m3_value.restype = ctypes.c_double
+    L.oracle_bf16_round.argtypes = [p, i64, p]
+    L.oracle_bf16_round.restype = None
+    L.oracle_block_sums.argtypes = [p, i64, ctypes.c_float, p, p, p, p]
+    L.oracle_block_sums.restype = None
+    return L
+
+
 def lib() -> ctypes.CDLL:
+    """The oracle library: the one built from ``nvfp4_oracle.c``, or the one
+    named by NVFP4_ORACLE_LIB (the mutation tests point it at copies of the
+    oracle with a planted mistake)."""
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(LIB_PATH)
-        p = ctypes.c_void_p
-        i64 = ctypes.c_int64
-        ci = ctypes.c_int
-        L.oracle_quantize.argtypes = [p, i64, i64, ci, ci, p, p, p, p, ci]
-        L.oracle_quantize.restype = ci
-        L.oracle_quantize_sampled.argtypes = [p, i64, i64, ci, ci, p, i64, p, p, p, ci]
-        L.oracle_quantize_sampled.restype = ci
-        L.oracle_dequantize.argtypes = [p, p, ctypes.c_float, i64, i64, p]
-        L.oracle_dequantize.restype = ci
-        L.oracle_mse.argtypes = [p, p, p, ctypes.c_float, i64]
-        L.oracle_mse.restype = ctypes.c_double
-        L.oracle_block_sse.argtypes = [p, p, p, ctypes.c_float, i64, p]
-        L.oracle_block_sse.restype = None
-        L.oracle_cjso_trace.argtypes = [p, i64, i64, ci, p, p]
-        L.oracle_cjso_trace.restype = ci
-        L.oracle_e2m1_encode.argtypes = [p, i64, p]
-        L.oracle_e2m1_encode.restype = None
-        L.oracle_e4m3_encode.argtypes = [p, i64, p]
-        L.oracle_e4m3_encode.restype = None
-        L.oracle_e4m3_floor_ceil.argtypes = [p, i64, p, p]
-        L.oracle_e4m3_floor_ceil.restype = None
-        L.oracle_e2m1_value.argtypes = [ci]
-        L.oracle_e2m1_value.restype = ctypes.c_double
-        L.oracle_e4m3_value.argtypes = [ci]
-        L.oracle_e4m3_value.restype = ctypes.c_double
-        L.oracle_bf16_round.argtypes = [p, i64, p]
-        L.oracle_bf16_round.restype = None
-        L.oracle_block_sums.argtypes = [p, i64, ctypes.c_float, p, p, p, p]
-        L.oracle_block_sums.restype = None
-        _lib = L
+        path = os.environ.get("NVFP4_ORACLE_LIB") or build()
+        _lib = load_library(path)
     return _lib
 
 
