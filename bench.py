@@ -67,7 +67,7 @@ WORKLOADS = {
 
 ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
 TWO_PASS = 4.5625   # B/elem: W read twice (alpha needs the global max first)
-DECOUPLED_FLOPS = 101 * 9  # per element: 101 candidates x (quotient 5 + P, R 4) fp32 flops
+DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P FMA 2 + R FMA 2)
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
@@ -85,7 +85,7 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
     if mode == 2:
         b = ONE_PASS if fits else (iters + 2) * 2 + 0.5625
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W stays in L2' if fits else f'{iters + 2} reads of W'})"
-    return "alu", "TFLOP/s", DECOUPLED_FLOPS * n, "909 fp32 flop/elem (101 candidates x 9)"
+    return "alu", "TFLOP/s", DECOUPLED_FLOPS * n, "505 fp32 flop/elem (101 candidates x [1 FMUL + 2 FMA])"
 
 
 # --------------------------------------------------------------------------- clocks
@@ -377,12 +377,15 @@ def run_ours(args, modes):
         bound, unit, work, rule = algorithmic(m, args.iters, n, l2)
         if bound == "hbm":
             achieved, peak, pk = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind
-        else:
-            achieved = work / (call_ms / 1e3) / 1e12
+            over = "the whole call"
+        else:  # the search kernel alone (its event-bracketed duration), not the CJSO sweeps before it
+            kc, kt = rep["k_decoupled"]
+            achieved = work / (kt / kc / 1e3) / 1e12
             peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
+            over = "k_decoupled"
         per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "us_per_call": call_ms * 1e3,
                           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule},
+                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over},
                           "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
                                                       for kn, (c, t) in rep.items()}}
     heavy = max(per_mode, key=lambda k: per_mode[k]["us_per_call"])
@@ -391,11 +394,13 @@ def run_ours(args, modes):
     out["roofline"] = {"bound": hr["bound"], "achieved": hr["achieved"], "peak": hr["peak"], "unit": hr["unit"],
                        "frac": hr["frac"],
                        "traffic": recorded_traffic(f"nvfp4_quantize({heavy})@{args.workload}"),
-                       "kernel": f"nvfp4_quantize({heavy}) = "
-                                 + " + ".join(per_mode[heavy]["kernels_event_bracketed"]),
+                       "kernel": (f"nvfp4_quantize({heavy}) = "
+                                  + " + ".join(per_mode[heavy]["kernels_event_bracketed"])
+                                  if hr["over"] == "the whole call" else hr["over"]),
                        "peak_kind": hr["peak_kind"], "rule": hr["rule"],
-                       "timing": "CUDA events on the launching stream around CUDA-graph replays of the call "
-                                 "alone (its kernels back to back)"}
+                       "timing": ("CUDA events on the launching stream around CUDA-graph replays of the call "
+                                  "alone (its kernels back to back)" if hr["over"] == "the whole call" else
+                                  "the library's CUDA events around each launch of the kernel, on its stream")}
 
     # ---- end to end through the C ABI with pinned host buffers
     W_pin = W_host.pin_memory()
@@ -441,6 +446,181 @@ def run_ours(args, modes):
     return out if rank == 0 else None
 
 
+# --------------------------------------------------------------------------- model-stack workload
+
+MODEL = "llama3_8b"
+MODEL_DESC = ("224 bf16 tensors of a Llama-3-8B-shaped stack (32 layers x {q 4096x4096, k/v 1024x4096, "
+              "o 4096x4096, gate/up 14336x4096, down 4096x14336}), Student-t df=5 std 0.02, generated on the "
+              "device with torch.Generator seeded 1000 + tensor index")
+
+
+def model_tensors(dev):
+    """The stack's tensors, generated on the device (Student-t df=5 scaled to std 0.02)."""
+    import torch
+    shapes = _synth().llama3_8b_shapes()
+    scale = 0.02 / math.sqrt(5.0 / 3.0)
+    Ws = []
+    for idx, (_, r, c) in enumerate(shapes):
+        g = torch.Generator(device=dev).manual_seed(1000 + idx)
+        z = torch.randn((r, c), generator=g, device=dev)
+        chi2 = 2.0 * torch._standard_gamma(torch.full((r, c), 2.5, device=dev), generator=g)
+        Ws.append((z * torch.rsqrt(chi2 / 5.0) * scale).to(torch.bfloat16))
+        del z, chi2
+    return shapes, Ws
+
+
+def run_model(args, modes):
+    import torch
+
+    import nvfp4_block_scale_gb300 as nv
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    shapes, Ws = model_tensors(dev)
+    ns = [W.numel() for W in Ws]
+    n = sum(ns)
+    outs = [(torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
+             torch.empty((r, c // 16), dtype=torch.uint8, device=dev),
+             torch.empty(1, dtype=torch.float32, device=dev)) for (_, r, c) in shapes]
+    qmodes = [m for m in modes if m != "dequant"]
+    mids = [MODE_IDS[m] for m in qmodes]
+
+    def grouped(mode):
+        nv.quantize_grouped(Ws, mode, args.iters, outs=outs)
+
+    def per_tensor(mode):
+        for W, o in zip(Ws, outs):
+            nv.quantize(W, mode, args.iters, out=o)
+
+    def step():
+        for m in mids:
+            grouped(m)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def event_ms(fn, k):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    gstep = graph_of(step)
+    clocks = ClockSampler(local)
+    for attempt in range(2):
+        clocks.start()
+        ms = event_ms(gstep.replay, args.steps)
+        clocks.stop()
+        csum = clocks.summary()
+        if not (set(csum.get("reasons", [])) & BAD_REASONS):
+            break
+        csum["remeasured"] = True
+    value = len(mids) * 2 * n * args.steps / (ms / 1e3) / 1e9
+    launches = 0
+    for m in mids:
+        launches += 2 * math.ceil(len(Ws) / nv.NVFP4_GROUP_MAX) if m in (0, 1) else \
+            len(Ws) * kernels_per_call(m, args.iters)
+    out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
+           "config": {"workload": MODEL, "desc": MODEL_DESC, "tensors": len(Ws), "elements": n,
+                      "modes": list(qmodes), "cjso_iters": args.iters if any(m >= 2 for m in mids) else None,
+                      "l2": f"inputs {2 * n >> 30} GiB, larger than L2 ({l2 >> 20} MiB)",
+                      "launch": "cuda_graph of nvfp4_quantize_grouped per mode",
+                      "parallelism": "1 GPU"},
+           "gpu_launches": launches * args.steps, "clocks": csum}
+
+    peak_hbm, peak_kind = measured_peaks()
+    sm_mhz = csum.get("sm_mhz") or 1900.0
+    per_mode = {}
+    for name, m in zip(qmodes, mids):
+        k = 3 if m >= 2 else 20
+        gm = graph_of(lambda: grouped(m))
+        call_ms = event_ms(gm.replay, k) / k
+        gp = graph_of(lambda: per_tensor(m))
+        per_tensor_ms = event_ms(gp.replay, k) / k
+        del gm, gp
+        nv.nvfp4_profiler_reset()
+        nv.nvfp4_profiler_enable(1)
+        grouped(m)
+        torch.cuda.synchronize()
+        nv.nvfp4_profiler_enable(0)
+        rep = nv.profiler_report()
+        if m in (0, 1):  # per tensor: one HBM read when it fits in half of L2, else two
+            work = sum((ONE_PASS if 2 * x <= l2 // 2 else TWO_PASS) * x for x in ns)
+            achieved, peak, pk, unit, bound = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind, "GB/s", "hbm"
+            rule, over = "2.5625 B/elem for tensors <= L2/2, 4.5625 above", "the whole call"
+        elif m == 2:
+            work = sum(((args.iters + 2) * 2 + 0.5625) * x for x in ns)
+            achieved, peak, pk, unit, bound = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind, "GB/s", "hbm"
+            rule, over = f"{(args.iters + 2) * 2 + 0.5625} B/elem ({args.iters + 2} reads of W)", "the whole call"
+        else:
+            kc, kt = rep["k_decoupled"]
+            work = DECOUPLED_FLOPS * n
+            achieved = work / (kt / 1e3) / 1e12
+            peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
+            unit, bound, over = "TFLOP/s", "alu", "k_decoupled (all tensors)"
+            rule = "505 fp32 flop/elem (101 candidates x [1 FMUL + 2 FMA])"
+        per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "ms_per_call": call_ms,
+                          "per_tensor_calls_ms": per_tensor_ms,
+                          "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over},
+                          "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
+                                                      for kn, (c, t) in rep.items()}}
+    heavy = max(per_mode, key=lambda x: per_mode[x]["ms_per_call"])
+    hr = per_mode[heavy]["roofline"]
+    out["per_mode"] = per_mode
+    out["roofline"] = dict(hr, traffic=recorded_traffic(f"nvfp4_quantize_grouped({heavy})@{MODEL}"),
+                           kernel=f"nvfp4_quantize_grouped({heavy})")
+
+    # end to end over layer 0 (7 tensors) through the C ABI with pinned host buffers
+    lay = list(range(7))
+    host_w = [Ws[i].cpu().pin_memory() for i in lay]
+    dev_w = [torch.empty_like(Ws[i]) for i in lay]
+    host_o = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[i]) for i in lay]
+    fos = MODE_IDS["four_over_six"]
+
+    def e2e_step():
+        for hw, dw in zip(host_w, dev_w):
+            dw.copy_(hw, non_blocking=True)
+        nv.quantize_grouped(dev_w, fos, 0, outs=[outs[i] for i in lay])
+        for i, ho in zip(lay, host_o):
+            for dst, src in zip(ho, outs[i]):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    k_e2e = 5
+    e2e_ms = event_ms(e2e_step, k_e2e)
+    n_lay = sum(ns[i] for i in lay)
+    out["e2e"] = {"value": 2 * n_lay * k_e2e / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "modes": ["four_over_six"],
+                  "sample": "layer 0 (7 tensors, 416 MiB), FourOverSix",
+                  "h2d_bytes_per_step": 2 * n_lay,
+                  "d2h_bytes_per_step": sum(t.numel() * t.element_size() for ho in host_o for t in ho),
+                  "steps": k_e2e}
+    w0 = Ws[0][:64].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    out["cpu_baseline"] = oracle_cpu_baseline(w0, qmodes, args.iters)
+    out["cpu_baseline"]["sample"] += " (layer 0 q_proj)"
+    return out
+
+
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args, modes):
@@ -448,9 +628,14 @@ def run_reference(args, modes):
     if rank != 0:
         return None
     import oracle
-    make, desc, _ = WORKLOADS[args.workload]
-    w_bits = make(0)
+    if args.workload == MODEL:  # the stack's first tensor (numpy recipe of the same distribution)
+        w_bits, desc = _synth().llama3_8b_tensor(0), MODEL_DESC
+    else:
+        make, desc, _ = WORKLOADS[args.workload]
+        w_bits = make(0)
     rows = max(16, min(w_bits.shape[0], (1 << 21) // w_bits.shape[1]))
+    if any(m == "cjso_decoupled" for m in modes):
+        rows = max(16, min(rows, (1 << 18) // w_bits.shape[1]))
     sample = w_bits[:rows]  # bounded per-step sample of the workload
     threads = os.cpu_count() or 1
 
@@ -485,17 +670,23 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + [MODEL])
     ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
     ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
-    modes = tuple(args.modes.split(",")) if args.modes else WORKLOADS[args.workload][2]
+    default_modes = ("four_over_six", "cjso_decoupled") if args.workload == MODEL else WORKLOADS[args.workload][2]
+    modes = tuple(args.modes.split(",")) if args.modes else default_modes
     for m in modes:
         if m not in MODE_IDS:
             raise SystemExit(f"unknown mode {m}")
-    out = run_reference(args, modes) if args.impl == "reference" else run_ours(args, modes)
+    if args.impl == "reference":
+        out = run_reference(args, modes)
+    elif args.workload == MODEL:
+        out = run_model(args, modes)
+    else:
+        out = run_ours(args, modes)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -93,6 +93,40 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
                    uint8_t *codes, uint8_t *scales, float *alpha, cudaStream_t stream);
 
 /*
+ * nvfp4_quantize_grouped -- quantize a list of tensors, each exactly as
+ *   nvfp4_quantize would (its own alpha from its own max|W|, [SOAR] quantizer
+ *   equation), with one pair of launches for up to NVFP4_GROUP_MAX tensors of
+ *   the max rule or FourOverSix: the first finds every tensor's max|W|, the
+ *   second quantizes every block of every tensor.  The pages quantize one
+ *   weight tensor at a time; this is a batching of that operation for a whole
+ *   model's weights, where per-tensor launches and the latency of small
+ *   tensors would otherwise dominate.
+ * Arguments:
+ *   tensors host array of `count` descriptors (read during the call only);
+ *           each descriptor's W, rows, cols, codes, scales and alpha follow
+ *           the rules of nvfp4_quantize.  Outputs of different tensors must
+ *           not overlap each other or any W.
+ *   count   >= 0 (0: nothing is enqueued).  Longer lists are processed in
+ *           consecutive slices of NVFP4_GROUP_MAX tensors.
+ *   mode, iters, stream  as for nvfp4_quantize.  Modes 2 and 3 run the
+ *           nvfp4_quantize launch sequence tensor by tensor (their search and
+ *           sweeps, not launches, dominate).
+ * Every descriptor is checked before anything is enqueued; the first bad one
+ * decides the returned status.
+ */
+#define NVFP4_GROUP_MAX 256
+typedef struct nvfp4_tensor {
+  const void *W;
+  int64_t rows;
+  int64_t cols;
+  uint8_t *codes;
+  uint8_t *scales;
+  float *alpha;
+} nvfp4_tensor;
+int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int iters,
+                           cudaStream_t stream);
+
+/*
  * nvfp4_dequantize -- codes, scales, alpha -> bf16 out [rows, cols],
  *   out = bf16_rne(q * fl(alpha * Delta_i)).  [SOAR] dequantization equation;
  *   one path for every scale rule ([FOS] section 02: no kernel change).

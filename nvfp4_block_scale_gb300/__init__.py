@@ -20,8 +20,15 @@ MAX, FOUR_OVER_SIX, CJSO, CJSO_DECOUPLED = 0, 1, 2, 3
 MODES = {"max": MAX, "four_over_six": FOUR_OVER_SIX, "cjso": CJSO, "cjso_decoupled": CJSO_DECOUPLED}
 
 NVFP4_OK = 0
+NVFP4_GROUP_MAX = 256
 
 _lib = None
+
+
+class nvfp4_tensor(ctypes.Structure):
+    """One descriptor of nvfp4_quantize_grouped (include/nvfp4.h)."""
+    _fields_ = [("W", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("alpha", ctypes.c_void_p)]
 
 
 class Nvfp4Error(RuntimeError):
@@ -49,6 +56,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_encode_e2m1.restype = ci
     L.nvfp4_encode_e4m3.argtypes = [vp, i64, vp, vp]
     L.nvfp4_encode_e4m3.restype = ci
+    L.nvfp4_quantize_grouped.argtypes = [ctypes.POINTER(nvfp4_tensor), ci, ci, ci, vp]
+    L.nvfp4_quantize_grouped.restype = ci
     L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp]
     L.nvfp4_quantize_noalloc.restype = ci
     L.nvfp4_profiler_enable.argtypes = [ci]
@@ -80,6 +89,11 @@ def nvfp4_quantize_noalloc(W, rows, cols, mode, codes, scales, alpha, stream) ->
     """Allocation-free max-rule / FourOverSix quantize (see include/nvfp4.h):
     for callers that must not let the library allocate device memory."""
     return load().nvfp4_quantize_noalloc(W, rows, cols, mode, codes, scales, alpha, stream)
+
+
+def nvfp4_quantize_grouped(tensors, count, mode, iters, stream) -> int:
+    """`tensors`: a ctypes array of nvfp4_tensor (or None with count 0)."""
+    return load().nvfp4_quantize_grouped(tensors, count, mode, iters, stream)
 
 
 def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
@@ -164,6 +178,31 @@ def quantize(W, mode=MAX, iters: int = 0, out=None, stream=None):
                         alpha.data_ptr(), _stream_ptr(stream))
     _check(st, "nvfp4_quantize")
     return codes, scales, alpha
+
+
+def quantize_grouped(Ws, mode=MAX, iters: int = 0, outs=None, stream=None):
+    """Quantizes a list of contiguous 2-D bf16 CUDA tensors with one grouped
+    call; returns a list of (codes, scales, alpha) as `quantize` does."""
+    import torch
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    res = []
+    arr = (nvfp4_tensor * max(1, len(Ws)))()
+    for i, W in enumerate(Ws):
+        if W.dtype != torch.bfloat16 or not W.is_cuda or W.dim() != 2 or not W.is_contiguous():
+            raise ValueError("every W must be a contiguous 2-D bf16 CUDA tensor")
+        rows, cols = W.shape
+        if outs is None:
+            o = (torch.empty((rows, cols // 2), dtype=torch.uint8, device=W.device),
+                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=W.device),
+                 torch.empty(1, dtype=torch.float32, device=W.device))
+        else:
+            o = outs[i]
+        arr[i] = nvfp4_tensor(W.data_ptr(), rows, cols, o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr())
+        res.append(o)
+    _check(nvfp4_quantize_grouped(arr, len(Ws), int(mode), int(iters), _stream_ptr(stream)),
+           "nvfp4_quantize_grouped")
+    return res
 
 
 def dequantize(codes, scales, alpha, rows: int, cols: int, out=None, stream=None):

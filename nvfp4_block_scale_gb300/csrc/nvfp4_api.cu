@@ -8,12 +8,17 @@
 //                       (each folds the previous sweep's partial sums)
 //   decoupled CJSO(T) : the CJSO(T) sweeps without codes -> decoupled search
 //   dequantize        : one kernel
+//   grouped max / FourOverSix: per slice of up to kGroupMax tensors, one
+//                       amax launch and one quantize launch for all of them
+//                       (after one memset of the slices' max|W| words)
 // Grid-wide dependencies are kernel boundaries: no kernel waits on another
 // CTA, so nothing can spin.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "../../include/nvfp4.h"
@@ -32,7 +37,7 @@ struct DevInfo {
   int status = NVFP4_OK;
   int sms = 0;
   int l2 = 0;  // L2 bytes
-  int occ[6] = {1, 1, 1, 1, 1, 1};
+  int occ[kKernCount] = {};
   cudaMemPool_t pool = nullptr;
 };
 
@@ -67,7 +72,7 @@ int device_info(DevInfo **out) {
     } else {
       e = prepare_decoupled_kernel();
       if (e != cudaSuccess) return map_cuda(e);
-      for (int k = 0; k < 6; ++k) d.occ[k] = max_active_ctas(k);
+      for (int k = 0; k < kKernCount; ++k) d.occ[k] = max_active_ctas(k);
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
       props.location.type = cudaMemLocationTypeDevice;
@@ -108,10 +113,11 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
-       kTrKinds };
+       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrKinds };
 const char *const kTraceNames[kTrKinds] = {"k_amax_partials",    "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
                                            "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
-                                           "k_dequant",           "k_encode"};
+                                           "k_dequant",           "k_encode",             "k_group_amax",
+                                           "k_group_quant<max>",  "k_group_quant<fos>"};
 
 struct TraceRec {
   int kind;
@@ -234,6 +240,73 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
     }
   }
   // The scratch goes back to the pool in stream order, after the last kernel.
+  cudaError_t ef = cudaFreeAsync(ws, stream);
+  return map_cuda(e != cudaSuccess ? e : ef);
+}
+
+int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int iters, cudaStream_t stream) {
+  if (count < 0 || (count > 0 && !tensors)) return NVFP4_ERR_INVALID_ARG;
+  if (mode < kModeMax || mode > kModeCjsoDecoupled) return NVFP4_ERR_INVALID_ARG;
+  const bool cjso = mode == kModeCjso || mode == kModeCjsoDecoupled;
+  if (cjso && (iters < 0 || iters > kMaxIters)) return NVFP4_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {  // every descriptor before anything is enqueued
+    const nvfp4_tensor &x = tensors[i];
+    int st = check_shape(x.rows, x.cols);
+    if (st != NVFP4_OK) return st;
+    const int64_t n = x.rows * x.cols;
+    if (!x.alpha || (n > 0 && (!x.W || !x.codes || !x.scales))) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x.alpha, 4) || (n > 0 && (!aligned(x.W, 16) || !aligned(x.codes, 4))))
+      return NVFP4_ERR_MISALIGNED;
+  }
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (count == 0) return NVFP4_OK;
+  if (cjso) {
+    for (int i = 0; i < count; ++i) {
+      const nvfp4_tensor &x = tensors[i];
+      st = nvfp4_quantize(x.W, x.rows, x.cols, mode, iters, x.codes, x.scales, x.alpha, stream);
+      if (st != NVFP4_OK) return st;
+    }
+    return NVFP4_OK;
+  }
+
+  const int nslices = (count + kGroupMax - 1) / kGroupMax;
+  const size_t slot = (size_t)round_up(int64_t(kGroupMax) * 4, 256);
+  void *ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, slot * nslices, d->pool, stream);
+  if (e != cudaSuccess) return map_cuda(e);
+  e = cudaMemsetAsync(ws, 0, slot * nslices, stream);  // every tensor's max|W| word starts at 0
+  GroupArgs *g = new (std::nothrow) GroupArgs;
+  if (!g && e == cudaSuccess) e = cudaErrorMemoryAllocation;
+  const int kq = mode == kModeFourOverSix ? kKernGroupQuantFos : kKernGroupQuantMax;
+  const int64_t full = int64_t(d->sms) * std::min(d->occ[kKernGroupAmax], d->occ[kq]);
+  for (int s0 = 0; s0 < count && e == cudaSuccess; s0 += kGroupMax) {
+    g->count = std::min(kGroupMax, count - s0);
+    g->tile_begin[0] = 0;
+    for (int i = 0; i < g->count; ++i) {
+      const nvfp4_tensor &x = tensors[s0 + i];
+      GroupTensor &gt = g->t[i];
+      gt.W = x.W;
+      gt.codes = x.codes;
+      gt.scales = x.scales;
+      gt.alpha = x.alpha;
+      gt.B = x.rows * x.cols / 16;
+      g->tile_begin[i + 1] = g->tile_begin[i] + (gt.B + kGroupTile - 1) / kGroupTile;
+    }
+    const int64_t tiles = g->tile_begin[g->count];
+    const int grid = (int)std::max<int64_t>(1, std::min(full, tiles));
+    uint32_t *amax = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + slot * (s0 / kGroupMax));
+    {
+      TraceScope tr(kTrGroupAmax, stream);
+      e = launch_group_amax(*g, amax, grid, stream);
+    }
+    if (e == cudaSuccess) {
+      TraceScope tr(mode == kModeFourOverSix ? kTrGroupQuantFos : kTrGroupQuantMax, stream);
+      e = launch_group_quant(mode, *g, amax, grid, stream);
+    }
+  }
+  delete g;
   cudaError_t ef = cudaFreeAsync(ws, stream);
   return map_cuda(e != cudaSuccess ? e : ef);
 }

@@ -8,7 +8,27 @@
 namespace nvfp4 {
 
 enum { kModeMax = 0, kModeFourOverSix = 1, kModeCjso = 2, kModeCjsoDecoupled = 3 };
-enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDecoupled, kKernDequant };
+enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDecoupled, kKernDequant, kKernGroupAmax,
+       kKernGroupQuantMax, kKernGroupQuantFos, kKernCount };
+
+// A group of tensors for the grouped max-rule / FourOverSix kernels, passed by
+// value as the kernels' parameter.  Tensor t owns the virtual tiles
+// [tile_begin[t], tile_begin[t+1]) of kGroupTile blocks each (its last tile
+// may be partial; an empty tensor owns none).
+constexpr int kGroupMax = 256;
+constexpr int kGroupTile = 256;  // blocks per tile = threads per CTA of the quantize kernel
+struct GroupTensor {
+  const void *W;
+  uint8_t *codes;
+  uint8_t *scales;
+  float *alpha;
+  int64_t B;  // 16-element blocks
+};
+struct GroupArgs {
+  int count;
+  int64_t tile_begin[kGroupMax + 1];
+  GroupTensor t[kGroupMax];
+};
 
 cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
@@ -24,6 +44,8 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const fl
                     cudaStream_t st);
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
 cudaError_t launch_encode_e4m3(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
+cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st);
+cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *amax, int grid, cudaStream_t st);
 cudaError_t prepare_decoupled_kernel();
 int max_active_ctas(int which);
 

@@ -428,6 +428,169 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
 }
 
 // ---------------------------------------------------------------------------
+// a1-a4, a7 over a group of tensors (max rule and FourOverSix)
+// ---------------------------------------------------------------------------
+//
+// The group's tensors lie end to end in a virtual space of tiles of
+// kGroupTile blocks; no tile holds blocks of two tensors.  Both kernels give
+// CTA c the same tile range [T*c/G, T*(c+1)/G): the amax kernel walks it
+// upwards, the quantize kernel downwards, so each CTA re-reads first what it
+// read last (still in L2).  Per tensor: max|W| by atomicMax on a zeroed word,
+// alpha = max|W| / (6*448) [SOAR-Q], then the same per-block arithmetic as
+// k_quant_max_fos.
+static_assert(kGroupTile == kThreads, "one block per thread per tile");
+constexpr int kGroupAmaxTiles = 8;  // tiles per step of the amax walk: 16 loads in flight per thread
+
+// The tensor owning `tile` (tile < tile_begin[count]); skips empty tensors.
+__device__ __forceinline__ int group_find(const GroupArgs &g, int64_t tile) {
+  int lo = 0, hi = g.count;  // tile_begin[lo] <= tile < tile_begin[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (g.tile_begin[mid] <= tile) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads) k_group_amax(const __grid_constant__ GroupArgs g,
+                                                         uint32_t *__restrict__ amax) {
+  __shared__ uint32_t red[kWarps];
+  pdl_wait();  // W and the zeroed words may come from earlier work on the stream
+  pdl_launch_dependents();
+  const int64_t T = g.tile_begin[g.count];
+  int64_t tile = T * blockIdx.x / gridDim.x;
+  const int64_t end = T * (blockIdx.x + 1) / gridDim.x;
+  if (tile >= end) return;
+  int t = group_find(g, tile);
+  uint32_t m = 0u;
+  while (tile < end) {
+    while (tile >= g.tile_begin[t + 1]) ++t;  // (t + 1 <= count: tile < tile_begin[count])
+    const int64_t stop = min(end, g.tile_begin[t + 1]);
+    const int64_t nt = min((int64_t)kGroupAmaxTiles, stop - tile);
+    const uint4 *W = static_cast<const uint4 *>(g.t[t].W);
+    const int64_t H = 2 * g.t[t].B;  // 16-byte units of tensor t
+    const int64_t u0 = (tile - g.tile_begin[t]) * (2 * kGroupTile);
+    uint4 v[2 * kGroupAmaxTiles];
+#pragma unroll
+    for (int u = 0; u < 2 * kGroupAmaxTiles; ++u) {
+      const int64_t i = u0 + (int64_t)u * kThreads + threadIdx.x;
+      v[u] = (u < 2 * nt && i < H) ? __ldg(W + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 2 * kGroupAmaxTiles; ++u) {
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].x));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].y));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].z));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].w));
+    }
+    tile += nt;
+    if (tile >= stop) {  // this CTA's part of tensor t is done
+      m &= 0x7FFF7FFFu;
+      m = block_max_u32(max(m & 0xFFFFu, m >> 16), red);
+      if (threadIdx.x == 0 && m != 0u) atomicMax(amax + t, m);
+      m = 0u;
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant__ GroupArgs g,
+                                                          const uint32_t *__restrict__ amax) {
+  __shared__ float s_tab[128], r_tab[128], ev_tab[128];
+  __shared__ uint8_t c4_tab[128];
+  constexpr bool FOS = MODE == kModeFourOverSix;
+  const int64_t T = g.tile_begin[g.count];
+  const int64_t lo = T * blockIdx.x / gridDim.x;
+  int64_t tile = T * (blockIdx.x + 1) / gridDim.x - 1;  // walks down to lo
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  auto load = [&](int64_t tl, int tt, uint4 &x0, uint4 &x1) {
+    const int64_t b = (tl - g.tile_begin[tt]) * kGroupTile + threadIdx.x;
+    if (b < g.t[tt].B) {
+      const uint4 *W = static_cast<const uint4 *>(g.t[tt].W);
+      x0 = __ldg(W + 2 * b);
+      x1 = __ldg(W + 2 * b + 1);
+    } else {
+      x0 = z;
+      x1 = z;
+    }
+  };
+  int t = 0, tn = 0;  // tensors of the current and of the next tile
+  uint4 a0 = z, a1 = z, n0 = z, n1 = z;
+  if (tile >= lo) {
+    t = tn = group_find(g, tile);
+    load(tile, t, a0, a1);
+    if (tile - 1 >= lo) {
+      while (tile - 1 < g.tile_begin[tn]) --tn;
+      load(tile - 1, tn, n0, n1);
+    }
+  }
+  if (threadIdx.x < 128) {  // alpha-independent tables
+    const float ev = e4m3_value(threadIdx.x);
+    ev_tab[threadIdx.x] = ev;
+    if (FOS) c4_tab[threadIdx.x] = (uint8_t)e4m3_code(__fmul_rn(ev, 1.5f));  // [FOS-02]
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  if (blockIdx.x == 0)  // an empty tensor's alpha is 0, as in nvfp4_quantize
+    for (int i = threadIdx.x; i < g.count; i += kThreads)
+      if (g.t[i].B == 0) *g.t[i].alpha = 0.0f;
+
+  int cur = -1;  // tensor whose tables are loaded
+  float alpha = 0.0f, six_a = 0.0f, r6 = 0.0f;
+  for (; tile >= lo; --tile) {
+    int tm = tn;
+    uint4 m0 = z, m1 = z;
+    if (tile - 2 >= lo) {
+      while (tile - 2 < g.tile_begin[tm]) --tm;
+      load(tile - 2, tm, m0, m1);
+    }
+    if (t != cur) {  // uniform over the CTA
+      alpha = __fdiv_rn(__uint_as_float(amax[t] << 16), 2688.0f);  // [SOAR-Q] alpha = max|W| / (6*448)
+      six_a = __fmul_rn(alpha, 6.0f);
+      r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
+      __syncthreads();  // the previous tensor's tables are no longer read
+      if (threadIdx.x < 128) {
+        const float sv = __fmul_rn(alpha, ev_tab[threadIdx.x]);
+        s_tab[threadIdx.x] = sv;
+        r_tab[threadIdx.x] = sv > 0.0f ? __frcp_rn(sv) : 0.0f;
+      }
+      __syncthreads();
+      cur = t;
+    }
+    const GroupTensor &gt = g.t[t];
+    if (threadIdx.x == 0 && tile == g.tile_begin[t]) *gt.alpha = alpha;
+    const int64_t b = (tile - g.tile_begin[t]) * kGroupTile + threadIdx.x;
+    if (b < gt.B) {
+      Block16 blk;
+      const uint32_t am = unpack16(a0, a1, blk);
+      const uint32_t d6 = max_rule_code(am, six_a, r6);
+      uint32_t c0, c1, d = d6;
+      float P6, R6;
+      quant16<FOS>(blk, s_tab[d6], r_tab[d6], c0, c1, P6, R6);
+      if (FOS) {  // [FOS-02] keep scale_m4 iff its dequant error is strictly lower
+        const uint32_t d4 = c4_tab[d6];
+        uint32_t e0, e1;
+        float P4, R4;
+        quant16<true>(blk, s_tab[d4], r_tab[d4], e0, e1, P4, R4);
+        const bool use4 = cand_err(s_tab[d4], P4, R4) < cand_err(s_tab[d6], P6, R6);
+        d = use4 ? d4 : d6;
+        c0 = use4 ? e0 : c0;
+        c1 = use4 ? e1 : c1;
+      }
+      uint32_t *codes32 = reinterpret_cast<uint32_t *>(gt.codes);
+      codes32[2 * b] = c0;
+      codes32[2 * b + 1] = c1;
+      gt.scales[b] = (uint8_t)d;
+    }
+    a0 = n0;
+    a1 = n1;
+    n0 = m0;
+    n1 = m1;
+    t = tn;
+    tn = tm;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // a8: dequantize
 // ---------------------------------------------------------------------------
 
@@ -552,6 +715,27 @@ cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, 
                             reinterpret_cast<uint32_t *>(codes));
 }
 
+cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_group_amax, g, amax);
+}
+
+cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *amax, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (mode == kModeFourOverSix) return cudaLaunchKernelEx(&cfg, k_group_quant<kModeFourOverSix>, g, amax);
+  return cudaLaunchKernelEx(&cfg, k_group_quant<kModeMax>, g, amax);
+}
+
 cudaError_t prepare_decoupled_kernel() {
   return cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
 }
@@ -583,6 +767,13 @@ int max_active_ctas(int which) {
     case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
     case kKernDecoupled:
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kDecThreads, kDecTableBytes);
+      break;
+    case kKernGroupAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_amax, kThreads, 0); break;
+    case kKernGroupQuantMax:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_quant<kModeMax>, kThreads, 0);
+      break;
+    case kKernGroupQuantFos:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_quant<kModeFourOverSix>, kThreads, 0);
       break;
     default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_dequant, kThreads, 0); break;
   }

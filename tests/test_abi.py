@@ -75,3 +75,35 @@ def test_dequantize_and_encode_reject_bad_arguments():
 def test_binding_names_mirror_the_header():
     for n in declared_functions():
         assert callable(getattr(nv, n)), n
+
+
+def _descs(*specs):
+    arr = (nv.nvfp4_tensor * max(1, len(specs)))()
+    for i, (w, rows, cols, c, s, a) in enumerate(specs):
+        arr[i] = nv.nvfp4_tensor(w, rows, cols, c, s, a)
+    return arr
+
+
+def test_grouped_rejects_bad_descriptors_before_anything():
+    good = (A16, 4, 16, A16, A16, A16)
+    assert nv.nvfp4_quantize_grouped(None, 3, 0, 0, None) == INVALID         # null list
+    assert nv.nvfp4_quantize_grouped(_descs(good), -1, 0, 0, None) == INVALID  # negative count
+    assert nv.nvfp4_quantize_grouped(_descs(good), 1, 5, 0, None) == INVALID   # unknown mode
+    assert nv.nvfp4_quantize_grouped(_descs(good), 1, 2, 65, None) == INVALID  # CJSO iterations
+    # the bad descriptor sits after a good one: nothing may have been enqueued for the first
+    assert nv.nvfp4_quantize_grouped(_descs(good, (A16, 4, 17, A16, A16, A16)), 2, 1, 0, None) == INVALID
+    assert nv.nvfp4_quantize_grouped(_descs(good, (A16, 4, 16, A16, A16, None)), 2, 0, 0, None) == INVALID
+    assert nv.nvfp4_quantize_grouped(_descs(good, (None, 4, 16, A16, A16, A16)), 2, 0, 0, None) == INVALID
+    assert nv.nvfp4_quantize_grouped(_descs(good, (A16 + 8, 4, 16, A16, A16, A16)), 2, 0, 0, None) == MISALIGNED
+    assert nv.nvfp4_quantize_grouped(_descs(good, (A16, 4, 16, A16 + 1, A16, A16)), 2, 1, 0, None) == MISALIGNED
+    assert nv.nvfp4_quantize_grouped(_descs(good, (A16, 4, 16, A16, A16, A16 + 2)), 2, 0, 0, None) == MISALIGNED
+
+
+def test_grouped_descriptor_layout_matches_header():
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct nvfp4_tensor \{(.*?)\} nvfp4_tensor;", text, re.S).group(1)
+    names = re.findall(r"\b(\w+);", body)
+    assert names == [f[0] for f in nv.nvfp4_tensor._fields_]
+    assert ctypes.sizeof(nv.nvfp4_tensor) == 48
+    m = re.search(r"#define NVFP4_GROUP_MAX (\d+)", text)
+    assert int(m.group(1)) == nv.NVFP4_GROUP_MAX
