@@ -454,10 +454,10 @@ MODEL_DESC = ("224 bf16 tensors of a Llama-3-8B-shaped stack (32 layers x {q 409
               "device with torch.Generator seeded 1000 + tensor index")
 
 
-def model_tensors(dev):
+def model_tensors(dev, layers=32):
     """The stack's tensors, generated on the device (Student-t df=5 scaled to std 0.02)."""
     import torch
-    shapes = _synth().llama3_8b_shapes()
+    shapes = _synth().llama3_8b_shapes(layers)
     scale = 0.02 / math.sqrt(5.0 / 3.0)
     Ws = []
     for idx, (_, r, c) in enumerate(shapes):
@@ -480,7 +480,7 @@ def run_model(args, modes):
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(dev)
     l2 = props.L2_cache_size
-    shapes, Ws = model_tensors(dev)
+    shapes, Ws = model_tensors(dev, args.layers)
     ns = [W.numel() for W in Ws]
     n = sum(ns)
     outs = [(torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
@@ -540,12 +540,15 @@ def run_model(args, modes):
     out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
-           "config": {"workload": MODEL, "desc": MODEL_DESC, "tensors": len(Ws), "elements": n,
+           "config": {"workload": MODEL, "desc": MODEL_DESC, "layers": args.layers, "tensors": len(Ws),
+                      "elements": n,
                       "modes": list(qmodes), "cjso_iters": args.iters if any(m >= 2 for m in mids) else None,
                       "l2": f"inputs {2 * n >> 30} GiB, larger than L2 ({l2 >> 20} MiB)",
                       "launch": "cuda_graph of nvfp4_quantize_grouped per mode",
                       "parallelism": "1 GPU"},
            "gpu_launches": launches * args.steps, "clocks": csum}
+    if args.quick:
+        return out
 
     peak_hbm, peak_kind = measured_peaks()
     sm_mhz = csum.get("sm_mhz") or 1900.0
@@ -673,6 +676,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + [MODEL])
     ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
     ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
+    ap.add_argument("--layers", type=int, default=32, help=f"layers of the {MODEL} stack (1..32)")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
