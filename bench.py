@@ -41,7 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
 HEADLINE = "studentt_4k"
-MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4}
+MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5}
+CONSUMERS = ("dequant", "gemv")  # modes that read a quantized tensor instead of producing one
 
 
 def _synth():
@@ -62,7 +63,7 @@ WORKLOADS = {
                ("max", "four_over_six", "cjso", "cjso_decoupled")),
     "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
                 "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)",
-                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")),
+                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant", "gemv")),
 }
 
 ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
@@ -71,7 +72,7 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1}[mode]
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1}[mode]
 
 
 def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
@@ -82,6 +83,8 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W <= L2/2: one HBM read' if fits else 'W read twice'})"
     if mode == 4:  # dequantize: codes + scales in, bf16 out
         return "hbm", "GB/s", ONE_PASS * n, "2.5625 B/elem (codes 0.5 + scales 1/16 read, bf16 2 written)"
+    if mode == 5:  # one-vector W4A16 product: codes + scales once, x and y negligible
+        return "hbm", "GB/s", 0.5625 * n, "0.5625 B/elem (codes + scales read once; + x, y)"
     if mode == 2:
         b = ONE_PASS if fits else (iters + 2) * 2 + 0.5625
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W stays in L2' if fits else f'{iters + 2} reads of W'})"
@@ -241,17 +244,24 @@ def run_ours(args, modes):
     mids = [MODE_IDS[m] for m in modes]
     outs = {m: (torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
-                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids if m != 4}
+                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids if m < 4}
 
-    if 4 in mids:  # dequantize inputs: this tensor quantized (max rule) once per rotation slot
+    if 4 in mids or 5 in mids:  # consumer inputs: this tensor quantized (max rule) once per rotation slot
         dq_in = []
         for i in range(ncopy):
             c, sc, a = nv.quantize(Wd[i], nv.MAX)
             dq_in.append((c, sc, a))
         dq_out = [torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) for _ in range(ncopy)]
+        gx = torch.randn((1, cols), device=dev).to(torch.bfloat16)
+        gy = torch.empty((1, rows), dtype=torch.float32, device=dev)
 
     def call(mode, w, s):
-        if mode == 4:  # dequantize the slot of this W into that slot's output
+        if mode == 5:  # one-vector product with the slot's quantized tensor
+            i = next(k for k in range(ncopy) if Wd[k] is w)
+            c, sc, a = dq_in[i]
+            st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), 1,
+                               gy.data_ptr(), s.cuda_stream)
+        elif mode == 4:  # dequantize the slot of this W into that slot's output
             i = next(k for k in range(ncopy) if Wd[k] is w)
             c, sc, a = dq_in[i]
             st = nv.nvfp4_dequantize(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, dq_out[i].data_ptr(),
@@ -405,7 +415,7 @@ def run_ours(args, modes):
     # ---- end to end through the C ABI with pinned host buffers
     W_pin = W_host.pin_memory()
     Wd0 = torch.empty_like(Wd[0])
-    qmids = [m for m in mids if m != 4]
+    qmids = [m for m in mids if m < 4]
     host_outs = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m]) for m in qmids}
 
     def e2e_step():
@@ -433,12 +443,12 @@ def run_ours(args, modes):
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     d2h = sum(t.numel() * t.element_size() for m in host_outs for t in host_outs[m])
     out["e2e"] = {"value": ws * len(qmids) * 2 * n * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
-                  "modes": [m for m in modes if m != "dequant"],
+                  "modes": [m for m in modes if m not in CONSUMERS],
                   "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e}
 
     if rank == 0 and ws == 1:
         rows_cap = None if n <= (1 << 24) else max(16, (1 << 22) // cols)
-        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, [m for m in modes if m != "dequant"], args.iters,
+        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, [m for m in modes if m not in CONSUMERS], args.iters,
                                                   max_rows=rows_cap)
     if ws > 1:
         dist.barrier()
@@ -486,7 +496,7 @@ def run_model(args, modes):
     outs = [(torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
              torch.empty((r, c // 16), dtype=torch.uint8, device=dev),
              torch.empty(1, dtype=torch.float32, device=dev)) for (_, r, c) in shapes]
-    qmodes = [m for m in modes if m != "dequant"]
+    qmodes = [m for m in modes if m not in CONSUMERS]
     mids = [MODE_IDS[m] for m in qmodes]
 
     def grouped(mode):
@@ -642,7 +652,7 @@ def run_reference(args, modes):
     sample = w_bits[:rows]  # bounded per-step sample of the workload
     threads = os.cpu_count() or 1
 
-    qmodes = [m for m in modes if m != "dequant"]
+    qmodes = [m for m in modes if m not in CONSUMERS]
 
     def step():
         for m in qmodes:

@@ -140,6 +140,30 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *a
                      int64_t rows, int64_t cols, void *out, cudaStream_t stream);
 
 /*
+ * nvfp4_gemv -- the W4A16 product that consumes a quantized tensor:
+ *   y[b][r] = sum_c What[r][c] * x[b][c] for b < batch, with What the
+ *   dequantized weights exactly as nvfp4_dequantize writes them
+ *   (bf16_rne(q * fl(alpha * Delta_i)), [SOAR] dequantization equation) and
+ *   fp32 accumulation (each product of two bf16 values is exact; the sum's
+ *   order is fixed, so results repeat bit for bit).  One kernel for every
+ *   scale rule ([FOS] section 02: the dequantization path is unchanged).
+ *   The pages quantize weights for such a decode kernel; the product itself
+ *   is the consumer of the path, not a step of it.
+ * Arguments:
+ *   codes, scales, alpha  a quantized [rows, cols] tensor as nvfp4_quantize
+ *          writes it (device; codes 8-byte aligned).
+ *   rows, cols  as for nvfp4_quantize.
+ *   x      device, bf16, 16-byte aligned, row-major [batch, cols].
+ *   batch  1..8 activation vectors.
+ *   y      device, fp32, 4-byte aligned, row-major [batch, rows] (written;
+ *          zeros when cols == 0).
+ *   stream cudaStream_t.
+ * Returns an nvfp4_status.
+ */
+int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
+               int64_t cols, const void *x, int batch, float *y, cudaStream_t stream);
+
+/*
  * nvfp4_encode_e2m1 -- element-wise fp32 -> E2M1 code (one code per output
  *   byte, sign in bit 3), rounding to nearest with ties to the even code and
  *   saturation at 6, exactly as the quantizer rounds x / (alpha * Delta).

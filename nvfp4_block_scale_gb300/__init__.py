@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_encode_e4m3.restype = ci
     L.nvfp4_quantize_grouped.argtypes = [ctypes.POINTER(nvfp4_tensor), ci, ci, ci, vp]
     L.nvfp4_quantize_grouped.restype = ci
+    L.nvfp4_gemv.argtypes = [vp, vp, vp, i64, i64, vp, ci, vp, vp]
+    L.nvfp4_gemv.restype = ci
     L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp]
     L.nvfp4_quantize_noalloc.restype = ci
     L.nvfp4_profiler_enable.argtypes = [ci]
@@ -98,6 +100,10 @@ def nvfp4_quantize_grouped(tensors, count, mode, iters, stream) -> int:
 
 def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
     return load().nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream)
+
+
+def nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream) -> int:
+    return load().nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream)
 
 
 def nvfp4_encode_e2m1(v, n, out, stream) -> int:
@@ -214,6 +220,21 @@ def dequantize(codes, scales, alpha, rows: int, cols: int, out=None, stream=None
                           _stream_ptr(stream))
     _check(st, "nvfp4_dequantize")
     return out
+
+
+def gemv(codes, scales, alpha, rows: int, cols: int, x, out=None, stream=None):
+    """y [batch, rows] fp32 = dequantized weights [rows, cols] times the bf16
+    activations x [batch, cols] (batch 1..8), on x's device."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.shape[1] != cols:
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [batch, cols]")
+    batch = x.shape[0]
+    y = out if out is not None else torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(nvfp4_gemv(codes.data_ptr(), scales.data_ptr(), alpha.data_ptr(), rows, cols, x.data_ptr(), batch,
+                      y.data_ptr(), _stream_ptr(stream)), "nvfp4_gemv")
+    return y
 
 
 def encode_e2m1(v, stream=None):

@@ -73,6 +73,8 @@ int device_info(DevInfo **out) {
       e = prepare_decoupled_kernel();
       if (e != cudaSuccess) return map_cuda(e);
       for (int k = 0; k < kKernCount; ++k) d.occ[k] = max_active_ctas(k);
+      e = prepare_gemv_kernels();
+      if (e != cudaSuccess) return map_cuda(e);
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
       props.location.type = cudaMemLocationTypeDevice;
@@ -113,11 +115,11 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
-       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrKinds };
+       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrKinds };
 const char *const kTraceNames[kTrKinds] = {"k_amax_partials",    "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
                                            "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
                                            "k_dequant",           "k_encode",             "k_group_amax",
-                                           "k_group_quant<max>",  "k_group_quant<fos>"};
+                                           "k_group_quant<max>",  "k_group_quant<fos>",   "k_gemv"};
 
 struct TraceRec {
   int kind;
@@ -325,6 +327,25 @@ int nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, const float *a
   const int64_t H = n / 8;
   TraceScope tr(kTrDequant, stream);
   return map_cuda(launch_dequant(codes, scales, alpha, H, out, grid_for(*d, kKernDequant, H), stream));
+}
+
+int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows, int64_t cols,
+               const void *x, int batch, float *y, cudaStream_t stream) {
+  int st = check_shape(rows, cols);
+  if (st != NVFP4_OK) return st;
+  if (batch < 1 || batch > 8) return NVFP4_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (!alpha || (n > 0 && (!codes || !scales || !x || !y))) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(alpha, 4) || (n > 0 && (!aligned(codes, 8) || !aligned(x, 16) || !aligned(y, 4))))
+    return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (rows == 0) return NVFP4_OK;
+  if (cols == 0) return map_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(rows * batch), stream));
+  TraceScope tr(kTrGemv, stream);
+  return map_cuda(launch_gemv(codes, scales, alpha, rows, cols, x, batch, y,
+                              gemv_grid(d->sms, batch, rows, cols), stream));
 }
 
 int nvfp4_encode_e2m1(const float *v, int64_t n, uint8_t *out, cudaStream_t stream) {

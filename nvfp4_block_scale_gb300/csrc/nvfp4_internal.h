@@ -46,6 +46,11 @@ cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid
 cudaError_t launch_encode_e4m3(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
 cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st);
 cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *amax, int grid, cudaStream_t st);
+cudaError_t launch_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows, int64_t cols,
+                        const void *x, int batch, float *y, int grid, cudaStream_t st);
+int gemv_grid(int sms, int batch, int64_t rows, int64_t cols);
+int gemv_max_active_ctas(int batch);
+cudaError_t prepare_gemv_kernels();
 cudaError_t prepare_decoupled_kernel();
 int max_active_ctas(int which);
 

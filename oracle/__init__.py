@@ -83,6 +83,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_bf16_round.restype = None
     L.oracle_block_sums.argtypes = [p, i64, ctypes.c_float, p, p, p, p]
     L.oracle_block_sums.restype = None
+    L.oracle_gemv.argtypes = [p, p, ctypes.c_float, i64, i64, p, ci, p]
+    L.oracle_gemv.restype = ci
     return L
 
 
@@ -231,3 +233,17 @@ def block_sums(w_bits, alpha: float, dcodes):
     Pe = np.zeros(nb, np.float64)
     lib().oracle_block_sums(_ptr(w), nb, ctypes.c_float(alpha), _ptr(dcodes), _ptr(P), _ptr(R), _ptr(Pe))
     return P, R, Pe
+
+
+def gemv(codes, scales, alpha: float, rows: int, cols: int, x_bits):
+    """y [batch, rows] (float64) = dequantized bf16 weights times bf16
+    activations x [batch, cols] (uint16 bit patterns), summed in double."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    x = np.ascontiguousarray(x_bits, np.uint16).reshape(-1, cols)
+    y = np.zeros((x.shape[0], rows), np.float64)
+    rc = lib().oracle_gemv(_ptr(codes), _ptr(scales), ctypes.c_float(alpha), rows, cols, _ptr(x), x.shape[0],
+                           _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_gemv failed")
+    return y

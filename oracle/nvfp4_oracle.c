@@ -57,6 +57,8 @@
  *       strict minimum of g in the order (k ascending, lower before upper)
  *       wins; alpha is not refitted after the search.
  *   R10 dequantized output is bf16_rne(fl(q * fl(alpha*Delta))).
+ *   R12 the W4A16 product (the consumer of the codes) multiplies the R10
+ *       bf16 weights by bf16 activations; the oracle sums in double.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC ... -lm -lpthread
  * (-ffp-contract=off: every float operation written here is rounded once,
@@ -678,4 +680,32 @@ void oracle_block_sums(const uint16_t *w, int64_t nblocks, float alpha, const ui
     for (int j = 0; j < BLOCK; ++j) p += fabs((double)x[j]) * E2M1_MAG[mag[j]];
     P_exact[b] = p;
   }
+}
+
+/* ---------------- consumer: W4A16 matrix-vector product ---------------- */
+
+/* y[b][r] = sum_c What[r][c] * x[b][c] in double, What = the dequantized
+ * bf16 weights of [SOAR-DQ] under reading R10 (the form a W4A16 kernel
+ * consumes), x bf16 [batch][cols]; y double [batch][rows].  Reading R12:
+ * the product consumes the dequantized weights rounded to bf16, exactly as
+ * oracle_dequantize writes them. */
+int oracle_gemv(const uint8_t *codes, const uint8_t *scales, float alpha, int64_t rows, int64_t cols,
+                const uint16_t *x, int batch, double *y) {
+  if (rows < 0 || cols < 0 || cols % BLOCK != 0 || batch < 1) return 1;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int b = 0; b < batch; ++b) {
+      double acc = 0.0;
+      for (int64_t c = 0; c < cols; ++c) {
+        int64_t i = r * cols + c;
+        int code = (codes[i / 2] >> (4 * (i & 1))) & 0xF;
+        float q = (float)E2M1_MAG[code & 7];
+        if (code & 8) q = -q;
+        float s = alpha * (float)e4m3_value(scales[i / BLOCK]);
+        double w = (double)bf16_to_f32(f32_to_bf16_rne(q * s));
+        acc += w * (double)bf16_to_f32(x[(int64_t)b * cols + c]);
+      }
+      y[(int64_t)b * rows + r] = acc;
+    }
+  }
+  return 0;
 }

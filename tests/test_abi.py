@@ -107,3 +107,18 @@ def test_grouped_descriptor_layout_matches_header():
     assert ctypes.sizeof(nv.nvfp4_tensor) == 48
     m = re.search(r"#define NVFP4_GROUP_MAX (\d+)", text)
     assert int(m.group(1)) == nv.NVFP4_GROUP_MAX
+
+
+@pytest.mark.parametrize("rows,cols,batch,expect", [
+    (4, 17, 1, INVALID), (-1, 16, 1, INVALID), (4, 16, 0, INVALID), (4, 16, 9, INVALID)])
+def test_gemv_rejects_bad_arguments(rows, cols, batch, expect):
+    assert nv.nvfp4_gemv(A16, A16, A16, rows, cols, A16, batch, A16, None) == expect
+
+
+def test_gemv_rejects_null_and_misaligned():
+    assert nv.nvfp4_gemv(None, A16, A16, 4, 16, A16, 1, A16, None) == INVALID
+    assert nv.nvfp4_gemv(A16, A16, None, 4, 16, A16, 1, A16, None) == INVALID
+    assert nv.nvfp4_gemv(A16, A16, A16, 4, 16, None, 1, A16, None) == INVALID
+    assert nv.nvfp4_gemv(A16 + 4, A16, A16, 4, 16, A16, 1, A16, None) == MISALIGNED  # codes: 8 bytes
+    assert nv.nvfp4_gemv(A16, A16, A16, 4, 16, A16 + 8, 1, A16, None) == MISALIGNED  # x: 16 bytes
+    assert nv.nvfp4_gemv(A16, A16, A16, 4, 16, A16, 1, A16 + 2, None) == MISALIGNED

@@ -354,3 +354,46 @@ def test_block_sums_exact(make):
         P, R, Pe = oracle.block_sums(w, alpha, dc.astype(np.uint8))
         assert np.array_equal(P.astype(np.float64), Pe)
         assert np.all(R * 4 == np.round(R * 4)) and np.all(R <= 576)
+
+
+# ------------------------------------------------------- W4A16 product (consumer)
+
+def _acts(batch, cols, seed):
+    rng = np.random.default_rng(seed)
+    return synthetic.to_bf16_bits(rng.standard_normal((batch, cols)).astype(np.float32))
+
+
+def test_gemv_on_representable_weights_is_the_plain_product():
+    """Round-trip-exact weights: the product equals W x of the original
+    weights, computed here in float64 from W itself."""
+    w, _, _ = representable_tensor(24, 256, 3)
+    codes, scales, alpha = oracle.quantize(w, oracle.MAX)
+    x = _acts(3, 256, 4)
+    y = oracle.gemv(codes, scales, alpha, 24, 256, x)
+    ref = f32(x).astype(np.float64) @ f32(w).astype(np.float64).T
+    bound = 1e-13 * (np.abs(f32(x)).astype(np.float64) @ np.abs(f32(w)).astype(np.float64).T)
+    assert np.all(np.abs(y - ref) <= bound)
+
+
+@pytest.mark.parametrize("mode,iters", [(0, 0), (1, 0), (2, 2), (3, 1)])
+def test_gemv_consumes_the_dequantized_bf16_weights(mode, iters):
+    """Every scale rule feeds the same product: y = dequantize(codes) x."""
+    w = synthetic.student_t(20, 320, 4.0, 0.02, 60 + mode)
+    codes, scales, alpha = oracle.quantize(w, mode, iters)
+    x = _acts(2, 320, 61)
+    y = oracle.gemv(codes, scales, alpha, 20, 320, x)
+    deq = f32(oracle.dequantize(codes, scales, alpha, 20, 320)).astype(np.float64)
+    ref = f32(x).astype(np.float64) @ deq.T
+    assert np.all(np.abs(y - ref) <= 1e-13 * (np.abs(f32(x)).astype(np.float64) @ np.abs(deq).T))
+
+
+def test_gemv_single_block_by_hand():
+    """1 x 16 weights [6, -3, 0.5, 0...] * 2^-12 (alpha exact, scale 448 for
+    the block maximum 6 * 448 * 2^-12... here a block of its own): y = sum w x."""
+    vals = np.zeros(16, np.float64)
+    vals[:3] = [6.0, -3.0, 0.5]
+    w = bf16_bits((vals * 448.0 * ALPHA_EXACT).reshape(1, 16))
+    codes, scales, alpha = oracle.quantize(w, oracle.MAX)
+    x = bf16_bits(np.r_[1.0, 2.0, 4.0, np.full(13, 3.0)].reshape(1, 16))
+    y = oracle.gemv(codes, scales, alpha, 1, 16, x)
+    assert y[0, 0] == (6.0 * 1 - 3.0 * 2 + 0.5 * 4) * 448.0 * ALPHA_EXACT

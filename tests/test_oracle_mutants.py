@@ -82,6 +82,12 @@ MUTANTS = [
                                                                "out[i] = (uint16_t)(u >> 16); }"),
     ("dequant_scale_by_block_of_8", "float s = alpha * (float)e4m3_value(scales[i / BLOCK]);\n    out",
      "float s = alpha * (float)e4m3_value(scales[i / 8]);\n    out"),
+    # W4A16 product
+    ("gemv_skips_bf16_rounding", "double w = (double)bf16_to_f32(f32_to_bf16_rne(q * s));", "double w = (double)(q * s);"),
+    ("gemv_activation_transposed", "acc += w * (double)bf16_to_f32(x[(int64_t)b * cols + c]);",
+     "acc += w * (double)bf16_to_f32(x[c * batch + b]);"),
+    ("gemv_output_transposed", "y[(int64_t)b * rows + r] = acc;", "y[r * batch + b] = acc;"),
+    ("gemv_drops_code_sign", "if (code & 8) q = -q;\n        float s = alpha", "float s = alpha"),
 ]
 
 PIN_FILES = [os.path.join(HERE, "test_oracle_method.py"), os.path.join(HERE, "test_oracle_formats.py")]
