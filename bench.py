@@ -41,8 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
 HEADLINE = "studentt_4k"
-MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5}
-CONSUMERS = ("dequant", "gemv")  # modes that read a quantized tensor instead of producing one
+MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5, "swizzle": 6}
+CONSUMERS = ("dequant", "gemv", "swizzle")  # modes that read a quantized tensor instead of producing one
 
 
 def _synth():
@@ -63,7 +63,7 @@ WORKLOADS = {
                ("max", "four_over_six", "cjso", "cjso_decoupled")),
     "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
                 "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)",
-                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant", "gemv")),
+                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant", "gemv", "swizzle")),
 }
 
 ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
@@ -72,7 +72,7 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1}[mode]
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1}[mode]
 
 
 def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
@@ -85,6 +85,8 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
         return "hbm", "GB/s", ONE_PASS * n, "2.5625 B/elem (codes 0.5 + scales 1/16 read, bf16 2 written)"
     if mode == 5:  # one-vector W4A16 product: codes + scales once, x and y negligible
         return "hbm", "GB/s", 0.5625 * n, "0.5625 B/elem (codes + scales read once; + x, y)"
+    if mode == 6:  # scale layout: scales read and written once
+        return "hbm", "GB/s", 0.125 * n, "0.125 B/elem (scales read + written)"
     if mode == 2:
         b = ONE_PASS if fits else (iters + 2) * 2 + 0.5625
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W stays in L2' if fits else f'{iters + 2} reads of W'})"
@@ -246,7 +248,7 @@ def run_ours(args, modes):
                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
                 torch.empty(1, dtype=torch.float32, device=dev)) for m in mids if m < 4}
 
-    if 4 in mids or 5 in mids:  # consumer inputs: this tensor quantized (max rule) once per rotation slot
+    if any(m >= 4 for m in mids):  # consumer inputs: this tensor quantized (max rule) once per rotation slot
         dq_in = []
         for i in range(ncopy):
             c, sc, a = nv.quantize(Wd[i], nv.MAX)
@@ -254,9 +256,13 @@ def run_ours(args, modes):
         dq_out = [torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) for _ in range(ncopy)]
         gx = torch.randn((1, cols), device=dev).to(torch.bfloat16)
         gy = torch.empty((1, rows), dtype=torch.float32, device=dev)
+        gz = torch.empty(nv.nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=dev)
 
     def call(mode, w, s):
-        if mode == 5:  # one-vector product with the slot's quantized tensor
+        if mode == 6:  # the slot's scales into the tensor-core layout
+            i = next(k for k in range(ncopy) if Wd[k] is w)
+            st = nv.nvfp4_swizzle_scales(dq_in[i][1].data_ptr(), rows, cols, gz.data_ptr(), s.cuda_stream)
+        elif mode == 5:  # one-vector product with the slot's quantized tensor
             i = next(k for k in range(ncopy) if Wd[k] is w)
             c, sc, a = dq_in[i]
             st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), 1,

@@ -164,6 +164,27 @@ int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
                int64_t cols, const void *x, int batch, float *y, cudaStream_t stream);
 
 /*
+ * nvfp4_swizzle_scales -- the E4M3 block scales of a quantized [rows, cols]
+ *   tensor, from the linear [rows, cols/16] layout that nvfp4_quantize
+ *   writes to the layout block-scaled tensor-core matrix multiplies read
+ *   (NVFP4 x NVFP4 GEMM inputs, 16-element blocks, E4M3 scales): the scale
+ *   matrix is padded with zeros to a multiple of 128 rows and 4 columns and
+ *   cut into 128 x 4 tiles stored one after another, column tiles varying
+ *   fastest; inside a tile the scale of row r (0..127) and column c (0..3)
+ *   is byte (r % 32) * 16 + (r / 32) * 4 + c.  The pages store the scales as
+ *   FP8 but fix no layout; this is the tensor-core one.  The codes need no
+ *   change (two per byte, even element in the low nibble, rows contiguous).
+ * Arguments: scales (device, rows*cols/16 bytes), rows/cols as for
+ *   nvfp4_quantize, out (device, 4-byte aligned,
+ *   nvfp4_swizzled_scales_bytes(rows, cols) bytes, written, padding zeroed),
+ *   stream.
+ * nvfp4_swizzled_scales_bytes returns that size, or -1 for an invalid shape.
+ */
+int64_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols);
+int nvfp4_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t cols, uint8_t *out,
+                         cudaStream_t stream);
+
+/*
  * nvfp4_encode_e2m1 -- element-wise fp32 -> E2M1 code (one code per output
  *   byte, sign in bit 3), rounding to nearest with ties to the even code and
  *   saturation at 6, exactly as the quantizer rounds x / (alpha * Delta).

@@ -60,6 +60,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_quantize_grouped.restype = ci
     L.nvfp4_gemv.argtypes = [vp, vp, vp, i64, i64, vp, ci, vp, vp]
     L.nvfp4_gemv.restype = ci
+    L.nvfp4_swizzled_scales_bytes.argtypes = [i64, i64]
+    L.nvfp4_swizzled_scales_bytes.restype = i64
+    L.nvfp4_swizzle_scales.argtypes = [vp, i64, i64, vp, vp]
+    L.nvfp4_swizzle_scales.restype = ci
     L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp]
     L.nvfp4_quantize_noalloc.restype = ci
     L.nvfp4_profiler_enable.argtypes = [ci]
@@ -104,6 +108,14 @@ def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
 
 def nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream) -> int:
     return load().nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream)
+
+
+def nvfp4_swizzled_scales_bytes(rows, cols) -> int:
+    return load().nvfp4_swizzled_scales_bytes(rows, cols)
+
+
+def nvfp4_swizzle_scales(scales, rows, cols, out, stream) -> int:
+    return load().nvfp4_swizzle_scales(scales, rows, cols, out, stream)
 
 
 def nvfp4_encode_e2m1(v, n, out, stream) -> int:
@@ -235,6 +247,15 @@ def gemv(codes, scales, alpha, rows: int, cols: int, x, out=None, stream=None):
     _check(nvfp4_gemv(codes.data_ptr(), scales.data_ptr(), alpha.data_ptr(), rows, cols, x.data_ptr(), batch,
                       y.data_ptr(), _stream_ptr(stream)), "nvfp4_gemv")
     return y
+
+
+def swizzle_scales(scales, rows: int, cols: int, stream=None):
+    """The [rows, cols/16] scales in the tensor-core tile layout (flat uint8)."""
+    import torch
+    out = torch.empty(nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=scales.device)
+    _check(nvfp4_swizzle_scales(scales.data_ptr(), rows, cols, out.data_ptr(), _stream_ptr(stream)),
+           "nvfp4_swizzle_scales")
+    return out
 
 
 def encode_e2m1(v, stream=None):

@@ -115,11 +115,12 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
-       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrKinds };
+       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrSwizzle, kTrKinds };
 const char *const kTraceNames[kTrKinds] = {"k_amax_partials",    "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
                                            "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
                                            "k_dequant",           "k_encode",             "k_group_amax",
-                                           "k_group_quant<max>",  "k_group_quant<fos>",   "k_gemv"};
+                                           "k_group_quant<max>",  "k_group_quant<fos>",   "k_gemv",
+                                           "k_swizzle_scales"};
 
 struct TraceRec {
   int kind;
@@ -346,6 +347,25 @@ int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   TraceScope tr(kTrGemv, stream);
   return map_cuda(launch_gemv(codes, scales, alpha, rows, cols, x, batch, y,
                               gemv_grid(d->sms, batch, rows, cols), stream));
+}
+
+int64_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols) {
+  if (check_shape(rows, cols) != NVFP4_OK) return -1;
+  return round_up(rows, 128) * round_up(cols / 16, 4);
+}
+
+int nvfp4_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t cols, uint8_t *out, cudaStream_t stream) {
+  int st = check_shape(rows, cols);
+  if (st != NVFP4_OK) return st;
+  const int64_t bytes = round_up(rows, 128) * round_up(cols / 16, 4);
+  if (bytes > 0 && (!scales || !out)) return NVFP4_ERR_INVALID_ARG;
+  if (bytes > 0 && !aligned(out, 4)) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (bytes == 0) return NVFP4_OK;
+  TraceScope tr(kTrSwizzle, stream);
+  return map_cuda(launch_swizzle_scales(scales, rows, cols / 16, out, stream));
 }
 
 int nvfp4_encode_e2m1(const float *v, int64_t n, uint8_t *out, cudaStream_t stream) {

@@ -51,6 +51,8 @@ cudaError_t launch_gemv(const uint8_t *codes, const uint8_t *scales, const float
 int gemv_grid(int sms, int batch, int64_t rows, int64_t cols);
 int gemv_max_active_ctas(int batch);
 cudaError_t prepare_gemv_kernels();
+cudaError_t launch_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t kb, uint8_t *out,
+                                  cudaStream_t st);
 cudaError_t prepare_decoupled_kernel();
 int max_active_ctas(int which);
 

@@ -617,6 +617,50 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint32_t *__restrict
 }
 
 // ---------------------------------------------------------------------------
+// scale layout for block-scaled tensor-core matrix multiplies
+// ---------------------------------------------------------------------------
+//
+// Linear [rows, kb] E4M3 scales -> tiles of 128 x 4 (zero padded), column
+// tiles fastest, scale (r, c) of a tile at byte (r % 32) * 16 + (r / 32) * 4
+// + c.  A CTA takes 128 rows x 64 scale columns (16 consecutive tiles, one
+// contiguous 8 KiB of output): it reads the rows' 64-byte segments
+// (consecutive threads, consecutive bytes) into shared memory and writes the
+// tiles' words in order.
+constexpr int kSwzCols = 64;  // scale columns per CTA = 16 tiles
+
+__global__ void __launch_bounds__(kThreads) k_swizzle_scales(const uint8_t *__restrict__ scales, int64_t rows,
+                                                             int64_t kb, uint32_t *__restrict__ out) {
+  __shared__ uint32_t tile[128][kSwzCols / 4 + 1];  // +1 word: rows fall in different banks
+  const int64_t ct = (kb + 3) / 4;                  // column tiles per row tile
+  const int64_t groups = (ct + 15) / 16;            // CTAs per row tile
+  const int64_t rt = blockIdx.x / groups, cg = blockIdx.x % groups;
+  const int64_t k0 = cg * kSwzCols;
+  if (kb % 4 == 0 && k0 + kSwzCols <= kb) {  // whole 4-byte words, each row 4-byte aligned
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(scales);
+    for (int e = threadIdx.x; e < 128 * (kSwzCols / 4); e += kThreads) {
+      const int r = e / (kSwzCols / 4), c = e % (kSwzCols / 4);
+      const int64_t row = rt * 128 + r;
+      tile[r][c] = row < rows ? __ldg(s32 + (row * kb + k0) / 4 + c) : 0u;
+    }
+  } else {
+    uint8_t *t8 = reinterpret_cast<uint8_t *>(&tile[0][0]);
+    for (int e = threadIdx.x; e < 128 * kSwzCols; e += kThreads) {
+      const int r = e / kSwzCols, c = e % kSwzCols;
+      const int64_t row = rt * 128 + r, k = k0 + c;
+      t8[r * (kSwzCols + 4) + c] = (row < rows && k < kb) ? __ldg(scales + row * kb + k) : (uint8_t)0;
+    }
+  }
+  __syncthreads();
+  const int64_t ntiles = min((int64_t)16, ct - cg * 16);
+  uint32_t *dst = out + (rt * ct + cg * 16) * 128;
+  for (int o = threadIdx.x; o < ntiles * 128; o += kThreads) {
+    const int t = o >> 7, within = o & 127;
+    const int r = (within & 3) * 32 + (within >> 2);
+    dst[o] = tile[r][t];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // element-wise format conversions (the quantizer's own rounding)
 // ---------------------------------------------------------------------------
 
@@ -745,6 +789,15 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const fl
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   return cudaLaunchKernelEx(&cfg, k_dequant, reinterpret_cast<const uint32_t *>(codes), scales, alpha, H,
                             static_cast<uint4 *>(out));
+}
+
+cudaError_t launch_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t kb, uint8_t *out,
+                                  cudaStream_t st) {
+  const int64_t ct = (kb + 3) / 4;
+  const int64_t ctas = (rows + 127) / 128 * ((ct + 15) / 16);
+  if (ctas > INT32_MAX) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = make_cfg((int)ctas, st);
+  return cudaLaunchKernelEx(&cfg, k_swizzle_scales, scales, rows, kb, reinterpret_cast<uint32_t *>(out));
 }
 
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st) {

@@ -85,6 +85,10 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_block_sums.restype = None
     L.oracle_gemv.argtypes = [p, p, ctypes.c_float, i64, i64, p, ci, p]
     L.oracle_gemv.restype = ci
+    L.oracle_swizzled_size.argtypes = [i64, i64]
+    L.oracle_swizzled_size.restype = i64
+    L.oracle_swizzle_scales.argtypes = [p, i64, i64, p]
+    L.oracle_swizzle_scales.restype = ci
     return L
 
 
@@ -247,3 +251,12 @@ def gemv(codes, scales, alpha: float, rows: int, cols: int, x_bits):
     if rc != 0:
         raise ValueError("oracle_gemv failed")
     return y
+
+
+def swizzle_scales(scales, rows: int, kb: int) -> np.ndarray:
+    """The [rows, kb] E4M3 scales in the tensor-core tile layout (flat uint8)."""
+    sc = np.ascontiguousarray(scales, np.uint8)
+    out = np.zeros(lib().oracle_swizzled_size(rows, kb), np.uint8)
+    if lib().oracle_swizzle_scales(_ptr(sc), rows, kb, _ptr(out)) != 0:
+        raise ValueError("oracle_swizzle_scales failed")
+    return out

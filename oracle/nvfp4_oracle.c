@@ -59,6 +59,9 @@
  *   R10 dequantized output is bf16_rne(fl(q * fl(alpha*Delta))).
  *   R12 the W4A16 product (the consumer of the codes) multiplies the R10
  *       bf16 weights by bf16 activations; the oracle sums in double.
+ *   R13 the tensor-core scale layout (tiles of 128 x 4 scales, 32 x 16
+ *       interleave inside a tile) is the one block-scaled matrix multiplies
+ *       read; the pages give none.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC ... -lm -lpthread
  * (-ffp-contract=off: every float operation written here is rounded once,
@@ -705,6 +708,34 @@ int oracle_gemv(const uint8_t *codes, const uint8_t *scales, float alpha, int64_
         acc += w * (double)bf16_to_f32(x[(int64_t)b * cols + c]);
       }
       y[(int64_t)b * rows + r] = acc;
+    }
+  }
+  return 0;
+}
+
+/* ---------------- scale layout for block-scaled tensor-core GEMMs ---------------- */
+
+/* Reading R13 (the pages store the E4M3 scales but give no layout): the
+ * layout block-scaled tensor-core matrix multiplies read.  The scale matrix
+ * [rows, kb] (kb = cols/16) is padded with zeros to multiples of 128 rows and
+ * 4 columns and cut into tiles of 128 x 4; tiles are stored one after the
+ * other, the column tile varying fastest; inside a tile, the scale of tile
+ * row r (0..127) and tile column c (0..3) sits at byte
+ * (r mod 32) * 16 + (r div 32) * 4 + c.  out: round_up(rows,128) *
+ * round_up(kb,4) bytes. */
+int64_t oracle_swizzled_size(int64_t rows, int64_t kb) {
+  return ((rows + 127) / 128 * 128) * ((kb + 3) / 4 * 4);
+}
+
+int oracle_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t kb, uint8_t *out) {
+  if (rows < 0 || kb < 0) return 1;
+  int64_t ct = (kb + 3) / 4;
+  memset(out, 0, (size_t)oracle_swizzled_size(rows, kb));
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t k = 0; k < kb; ++k) {
+      int64_t tile = (i / 128) * ct + k / 4;
+      int64_t r = i % 128, c = k % 4;
+      out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c] = scales[i * kb + k];
     }
   }
   return 0;

@@ -122,3 +122,12 @@ def test_gemv_rejects_null_and_misaligned():
     assert nv.nvfp4_gemv(A16 + 4, A16, A16, 4, 16, A16, 1, A16, None) == MISALIGNED  # codes: 8 bytes
     assert nv.nvfp4_gemv(A16, A16, A16, 4, 16, A16 + 8, 1, A16, None) == MISALIGNED  # x: 16 bytes
     assert nv.nvfp4_gemv(A16, A16, A16, 4, 16, A16, 1, A16 + 2, None) == MISALIGNED
+
+
+def test_swizzled_size_and_checks():
+    assert nv.nvfp4_swizzled_scales_bytes(300, 160) == 384 * 12
+    assert nv.nvfp4_swizzled_scales_bytes(128, 64) == 512
+    assert nv.nvfp4_swizzled_scales_bytes(4, 17) == -1
+    assert nv.nvfp4_swizzle_scales(A16, 4, 17, A16, None) == INVALID
+    assert nv.nvfp4_swizzle_scales(None, 4, 16, A16, None) == INVALID
+    assert nv.nvfp4_swizzle_scales(A16, 4, 16, A16 + 2, None) == MISALIGNED

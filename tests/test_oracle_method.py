@@ -397,3 +397,31 @@ def test_gemv_single_block_by_hand():
     x = bf16_bits(np.r_[1.0, 2.0, 4.0, np.full(13, 3.0)].reshape(1, 16))
     y = oracle.gemv(codes, scales, alpha, 1, 16, x)
     assert y[0, 0] == (6.0 * 1 - 3.0 * 2 + 0.5 * 4) * 448.0 * ALPHA_EXACT
+
+
+# ------------------------------------------------ tensor-core scale layout (R13)
+
+def test_swizzle_hand_worked_positions():
+    """Scales of a 300 x 10 (kb) matrix: tiles of 128 x 4, column tiles
+    fastest (3 per row of tiles), byte (r%32)*16 + (r//32)*4 + c inside."""
+    rows, kb = 300, 10
+    sc = (np.arange(rows * kb) % 251 + 1).astype(np.uint8).reshape(rows, kb)
+    out = oracle.swizzle_scales(sc, rows, kb)
+    assert out.size == 384 * 12
+    assert out[0] == sc[0, 0] and out[1] == sc[0, 1] and out[4] == sc[32, 0] and out[16] == sc[1, 0]
+    assert out[22 + 0] == sc[33, 2]                      # r = 33: 1*16 + 1*4 + 2
+    assert out[512 + 0] == sc[0, 4]                      # second column tile of the first row tile
+    assert out[3 * 512 + 5 * 16 + 3 * 4 + 1] == sc[128 + 96 + 5, 1]
+    assert out[8 * 512 + (299 % 32) * 16 + ((299 % 128) // 32) * 4 + 1] == sc[299, 9]
+
+
+def test_swizzle_is_a_padded_permutation():
+    rows, kb = 131, 7
+    sc = np.arange(1, rows * kb + 1, dtype=np.int64)
+    lo = (sc % 256).astype(np.uint8).reshape(rows, kb)
+    hi = (sc // 256).astype(np.uint8).reshape(rows, kb)
+    a, b = oracle.swizzle_scales(lo, rows, kb), oracle.swizzle_scales(hi, rows, kb)
+    ids = a.astype(np.int64) + 256 * b.astype(np.int64)
+    nz = ids[ids != 0]
+    assert np.array_equal(np.sort(nz), np.arange(1, rows * kb + 1))
+    assert ids.size == 256 * 8 and (ids == 0).sum() == 256 * 8 - rows * kb

@@ -87,6 +87,11 @@ MUTANTS = [
     ("gemv_activation_transposed", "acc += w * (double)bf16_to_f32(x[(int64_t)b * cols + c]);",
      "acc += w * (double)bf16_to_f32(x[c * batch + b]);"),
     ("gemv_output_transposed", "y[(int64_t)b * rows + r] = acc;", "y[r * batch + b] = acc;"),
+    # tensor-core scale layout
+    ("swizzle_row_tiles_fastest", "int64_t tile = (i / 128) * ct + k / 4;",
+     "int64_t tile = (k / 4) * ((rows + 127) / 128) + i / 128;"),
+    ("swizzle_interleave_swapped", "out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c]",
+     "out[tile * 512 + (r / 32) * 16 + (r % 32) * 4 + c]"),
     ("gemv_drops_code_sign", "if (code & 8) q = -q;\n        float s = alpha", "float s = alpha"),
 ]
 
