@@ -289,27 +289,35 @@ def run_ours(args, modes):
 
     launch = "eager"
     graphs = []
-    if not args.quick:  # one CUDA graph per rotation slot, each = one step
+    # steps per CUDA graph: back-to-back calls chain by programmatic dependent
+    # launch inside a graph, and the graph boundary costs a launch gap
+    per_graph = 8 if args.steps % 8 == 0 and not args.quick else 1
+    if not args.quick:  # ncopy CUDA graphs of `per_graph` consecutive steps each (the rotation continues)
         try:
             for i in range(ncopy):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
-                    step(i, torch.cuda.current_stream())
+                    for t in range(per_graph):
+                        step(i * per_graph + t, torch.cuda.current_stream())
                 graphs.append(g)
             for g in graphs:
                 g.replay()
             torch.cuda.synchronize()
-            launch = "cuda_graph"
+            launch = f"cuda_graph ({per_graph} step(s) per graph)"
         except Exception as e:  # eager fallback, reported in config
             launch = f"eager ({type(e).__name__})"
             graphs = []
 
-    def run_steps(k, s):
-        for i in range(k):
-            if graphs:
+    def run_steps(k, s):  # k steps (a multiple of per_graph when graphs are used)
+        if graphs:
+            for i in range(k // per_graph):
                 graphs[i % len(graphs)].replay()
-            else:
+        else:
+            for i in range(k):
                 step(i, s)
+
+    def whole(k):  # k rounded up to whole graphs
+        return -(-k // per_graph) * per_graph if graphs else k
 
     def timed(k):
         if ws > 1:
@@ -327,11 +335,11 @@ def run_ours(args, modes):
 
     clocks = ClockSampler(local)
     for attempt in range(2):
-        run_steps(max(args.warmup, 3), stream)
+        run_steps(whole(max(args.warmup, 3)), stream)
         clocks.start()
         ms = timed(args.steps)
         if len(clocks.samples) < 5 and not args.quick:  # short region: keep sampling over the same loop
-            timed(max(args.steps, int(200.0 / max(ms / args.steps, 1e-3))))
+            timed(whole(max(args.steps, int(200.0 / max(ms / args.steps, 1e-3)))))
         clocks.stop()
         csum = clocks.summary()
         if not (set(csum.get("reasons", [])) & BAD_REASONS):
@@ -361,26 +369,36 @@ def run_ours(args, modes):
     peak_hbm, peak_kind = measured_peaks()
     sm_mhz = csum.get("sm_mhz") or 1900.0
     for name, m in zip(modes, mids):
-        # device time of this mode alone: graph replays of one call per rotation slot
-        k = max(min(args.steps, 500), 20)
-        gm = []
-        if graphs:
-            for i in range(ncopy):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    call(m, Wd[i], torch.cuda.current_stream())
-                gm.append(g)
-        for i in range(ncopy):
-            (gm[i].replay() if gm else call(m, Wd[i], stream))
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(k):
-            (gm[i % ncopy].replay() if gm else call(m, Wd[i % ncopy], stream))
-        e1.record(stream)
-        torch.cuda.synchronize()
-        call_ms = e0.elapsed_time(e1) / k
+        # device time of this mode alone: graphs of 8 back-to-back calls on rotating
+        # copies (steady state), and graphs of one call (an isolated call's latency)
+        k = max(min(args.steps, 480), 24)
+        times = {}
+        for chain in (8, 1):
+            gm = []
+            if graphs:
+                for i in range(ncopy):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for t in range(chain):
+                            call(m, Wd[(i * chain + t) % ncopy], torch.cuda.current_stream())
+                    gm.append(g)
+            for g in gm:
+                g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if gm:
+                for i in range(k // chain):
+                    gm[i % ncopy].replay()
+            else:
+                for i in range(k):
+                    call(m, Wd[i % ncopy], stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[chain] = e0.elapsed_time(e1) / k
+            del gm
+        call_ms = times[8]
         # per-kernel breakdown from the library tracer (event-bracketed launches,
         # so each includes its launch gap)
         nv.nvfp4_profiler_reset()
@@ -400,6 +418,7 @@ def run_ours(args, modes):
             peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
             over = "k_decoupled"
         per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "us_per_call": call_ms * 1e3,
+                          "us_isolated_call": times[1] * 1e3,
                           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                                        "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over},
                           "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
@@ -414,8 +433,8 @@ def run_ours(args, modes):
                                   + " + ".join(per_mode[heavy]["kernels_event_bracketed"])
                                   if hr["over"] == "the whole call" else hr["over"]),
                        "peak_kind": hr["peak_kind"], "rule": hr["rule"],
-                       "timing": ("CUDA events on the launching stream around CUDA-graph replays of the call "
-                                  "alone (its kernels back to back)" if hr["over"] == "the whole call" else
+                       "timing": ("CUDA events on the launching stream around CUDA-graph replays of 8 calls "
+                                  "back to back on rotating inputs (per call)" if hr["over"] == "the whole call" else
                                   "the library's CUDA events around each launch of the kernel, on its stream")}
 
     # ---- end to end through the C ABI with pinned host buffers

@@ -33,6 +33,9 @@
  *   - Inputs must be finite, and either all zero or with max|W| >= 2^-64; for
  *     other inputs the outputs are unspecified (no memory is touched beyond
  *     the documented buffers either way).
+ *   - The first call on a device performs a one-time set-up with that
+ *     device current (device queries, kernel attributes, the library's
+ *     memory pool); make it before any stream capture (a warm-up call).
  *   - Calls on different streams may run concurrently; the library keeps no
  *     per-call global state.  Scratch memory comes from a library-owned,
  *     stream-ordered memory pool (cudaMallocFromPoolAsync / cudaFreeAsync on
