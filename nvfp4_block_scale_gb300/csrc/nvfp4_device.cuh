@@ -64,62 +64,10 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
   return __fmaf_rn(e, r, q0);
 }
 
-// bf16 pair in a 32-bit word -> floats (element 2k in the low half).
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // Error of a candidate scale minus the block's common sum x^2:
 // s * (s*R - 2P), as fl(s * fma(s, R, -2P)).
 __device__ __forceinline__ float cand_err(float s, float P, float R) {
   return __fmul_rn(s, __fmaf_rn(s, R, __fmul_rn(-2.0f, P)));
-}
-
-// Eight elements (half of a 16-element block) quantized with dequant scale s
-// and its reciprocal r: magnitude codes (nibble k = element k), P = sum |x| q
-// and R = sum q^2.  A zero scale gives zero codes and sums.
-struct HalfQ {
-  uint32_t mags;
-  float P, R;
-};
-
-__device__ __forceinline__ HalfQ quant_half(const float (&ax)[8], float s, float r) {
-  HalfQ o;
-  uint32_t mags = 0;
-  float P = 0.0f, R = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float v0 = div_by_scale(ax[2 * k], s, r);
-    float v1 = div_by_scale(ax[2 * k + 1], s, r);
-    uint32_t b = cvt_e2m1x2(v1, v0);
-    float2 q = e2m1x2_to_f32x2(b);
-    P = __fmaf_rn(ax[2 * k], q.x, P);
-    P = __fmaf_rn(ax[2 * k + 1], q.y, P);
-    R = __fmaf_rn(q.x, q.x, R);
-    R = __fmaf_rn(q.y, q.y, R);
-    mags |= b << (8 * k);
-  }
-  const bool live = s > 0.0f;
-  o.mags = live ? mags : 0u;
-  o.P = live ? P : 0.0f;
-  o.R = live ? R : 0.0f;
-  return o;
-}
-
-// Unpacks 8 bf16 (one uint4) into |x|, the sign nibble bits (bit 4k+3 = sign
-// of element k) and the largest |x| as bf16 bits (0..0x7FFF).
-__device__ __forceinline__ void unpack8(const uint4 &w, float (&ax)[8], uint32_t &sgn, uint32_t &amax_bits) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  sgn = 0;
-  amax_bits = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t a = ws[k] & 0x7FFF7FFFu;
-    ax[2 * k] = bf16_lo(a);
-    ax[2 * k + 1] = bf16_hi(a);
-    amax_bits = max(amax_bits, max(a & 0xFFFFu, a >> 16));
-    sgn |= ((ws[k] >> 15) & 1u) << (8 * k + 3);
-    sgn |= (ws[k] >> 31) << (8 * k + 7);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -369,62 +317,6 @@ __device__ __forceinline__ float cand_err_m2p(float s, float m2P, float R) {
 // are no-ops when the launch carries no programmatic dependency.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
-// Bulk (TMA) copies into shared memory, tracked by mbarriers.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-// Makes initialized mbarriers visible to the bulk-copy (async) proxy.
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Orders this thread's earlier generic-proxy shared-memory accesses before
-// later bulk-copy writes to the same memory.
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// One thread: expect `bytes` on `bar` and start the copy global -> shared.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// Waits for phase `parity` of `bar` to complete, giving up after `limit`
-// polls.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t it = 0; it < limit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
-  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 
 // Compensated (float, float) accumulator, ~48 significant bits.
 struct FF {

@@ -1,9 +1,10 @@
 // nvfp4_kernels.cu -- sm_103a kernels of the NVFP4 quantization hot path.
 //
-// Work unit: a "half block" = 8 consecutive bf16 = one 16-byte load.  Two
-// adjacent lanes of a warp hold one 16-element block and combine their block
-// amax and sums with one shuffle.  Warps walk the tensor in tiles of 32 half
-// blocks (512 contiguous bytes per warp per load: fully coalesced), grid-stride.
+// Work unit: one 16-element block (32 bytes of bf16, two 16-byte loads) per
+// thread; a warp's loads cover 1 KiB of contiguous W.  The amax pass reads W
+// as 16-byte units with 16 loads in flight per thread.  Per element the
+// quotient |x| / fl(alpha * Delta) is an IEEE fp32 division reproduced by one
+// packed Markstein step, and the code is the hardware E2M1 conversion of it.
 //
 // Citation keys (page title, part of the page):
 //   [SOAR-Q]   "SOAR: Scale Optimization for Accurate Reconstruction in NVFP4
