@@ -195,6 +195,22 @@ def recorded_traffic(key: str):
     return None
 
 
+def max_over_ranks(x: float, device, ws: int) -> float:
+    """The largest of every rank's x (each rank passes its own; ws == 1: x)."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(ws: int, bytes_per_step_per_rank: float, steps: int, ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return ws * bytes_per_step_per_rank * steps / (ms / 1e3) / 1e9
+
+
 def dist_env():
     return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -345,12 +361,9 @@ def run_ours(args, modes):
         if not (set(csum.get("reasons", [])) & BAD_REASONS):
             break
         csum["remeasured"] = True
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(ms, dev, ws)
     bytes_per_step = len(mids) * 2 * n
-    value = ws * bytes_per_step * args.steps / (ms / 1e3) / 1e9
+    value = job_gbs(ws, bytes_per_step, args.steps, ms)
     out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
@@ -463,11 +476,9 @@ def run_ours(args, modes):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev, ws)
     d2h = sum(t.numel() * t.element_size() for m in host_outs for t in host_outs[m])
-    out["e2e"] = {"value": ws * len(qmids) * 2 * n * k_e2e / (float(e2e_ms.item()) / 1e3) / 1e9, "unit": "GB/s",
+    out["e2e"] = {"value": job_gbs(ws, len(qmids) * 2 * n, k_e2e, e2e_ms), "unit": "GB/s",
                   "modes": [m for m in modes if m not in CONSUMERS],
                   "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e}
 
