@@ -115,12 +115,12 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
-       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrSwizzle, kTrKinds };
-const char *const kTraceNames[kTrKinds] = {"k_amax_partials",    "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
+       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrSwizzle, kTrAmaxLdg, kTrKinds };
+const char *const kTraceNames[kTrKinds] = {"k_amax_bulk",        "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
                                            "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
                                            "k_dequant",           "k_encode",             "k_group_amax",
                                            "k_group_quant<max>",  "k_group_quant<fos>",   "k_gemv",
-                                           "k_swizzle_scales"};
+                                           "k_swizzle_scales",   "k_amax_partials"};
 
 struct TraceRec {
   int kind;
@@ -198,7 +198,11 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int64_t H = n / 8;   // half blocks = 16-byte loads
   const int64_t B = n / 16;  // blocks
   const int T = cjso ? iters : 0;
-  const int g_amax = grid_for(*d, kKernAmax, H / 16 + 1);  // 16 loads per thread per tile
+  // amax pass: bulk copies through shared memory for tensors beyond half of L2
+  // (measured faster there), plain 16-byte loads for smaller ones (faster there)
+  const bool bulk = 2 * n > int64_t(d->l2) / 2;
+  const int g_amax = bulk ? (int)std::min<int64_t>(amax_bulk_chunks(H), int64_t(d->sms) * d->occ[kKernAmax])
+                          : grid_for(*d, kKernAmaxLdg, H / 16 + 1);  // 16 loads per thread per tile
   const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
@@ -219,8 +223,9 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   float *hist = reinterpret_cast<float *>(base + off_hist);
 
   {
-    TraceScope tr(kTrAmax, stream);
-    e = launch_amax_partials(W, H, amax_part, g_amax, stream);
+    TraceScope tr(bulk ? kTrAmax : kTrAmaxLdg, stream);
+    e = bulk ? launch_amax_bulk(W, H, amax_part, g_amax, stream)
+             : launch_amax_partials(W, H, amax_part, g_amax, stream);
   }
   if (e == cudaSuccess && !cjso) {
     TraceScope tr(mode == kModeFourOverSix ? kTrQuantFos : kTrQuantMax, stream);

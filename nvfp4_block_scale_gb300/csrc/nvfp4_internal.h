@@ -9,7 +9,7 @@ namespace nvfp4 {
 
 enum { kModeMax = 0, kModeFourOverSix = 1, kModeCjso = 2, kModeCjsoDecoupled = 3 };
 enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDecoupled, kKernDequant, kKernGroupAmax,
-       kKernGroupQuantMax, kKernGroupQuantFos, kKernCount };
+       kKernGroupQuantMax, kKernGroupQuantFos, kKernAmaxLdg, kKernCount };
 
 // A group of tensors for the grouped max-rule / FourOverSix kernels, passed by
 // value as the kernels' parameter.  Tensor t owns the virtual tiles
@@ -31,6 +31,8 @@ struct GroupArgs {
 };
 
 cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
+cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
+int amax_bulk_chunks(int64_t n16);
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
                                  cudaStream_t st);

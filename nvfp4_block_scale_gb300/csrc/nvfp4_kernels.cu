@@ -149,6 +149,97 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
   if (threadIdx.x == 0) part[blockIdx.x] = m;
 }
 
+// Bulk-copy form of the same pass: each CTA streams chunks c, c + G, ... of
+// kAmaxChunk bytes through kAmaxStages shared-memory stages filled by
+// cp.async.bulk (one elected thread issues, an mbarrier counts the bytes);
+// all threads reduce a stage, then it is refilled.  Every mbarrier wait is
+// bounded: on a timeout the CTA waits (bounded) for its copies in flight and
+// writes the partial 0xFFFFFFFF, which makes the quantize kernel's alpha NaN.
+constexpr int kAmaxStages = 4;
+constexpr int kAmaxChunk = 32768;
+constexpr size_t kAmaxBulkSmem = (size_t)kAmaxStages * kAmaxChunk;
+constexpr long kSpinLimit = 1L << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mb, uint32_t parity) {
+  uint32_t done = 0;
+  for (long it = 0; !done && it < kSpinLimit; ++it)
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(mb), "r"(parity) : "memory");
+  return done != 0;
+}
+
+__global__ void __launch_bounds__(kThreads) k_amax_bulk(const uint4 *__restrict__ W, int64_t n16,
+                                                        uint32_t *__restrict__ part) {
+  extern __shared__ __align__(128) uint4 stage[];  // kAmaxStages x kAmaxChunk bytes
+  __shared__ __align__(8) uint64_t mbar[kAmaxStages];
+  __shared__ uint32_t red[kWarps];
+  constexpr int64_t kUnits = kAmaxChunk / 16;
+  const int64_t nch = (n16 + kUnits - 1) / kUnits;
+  const char *src = reinterpret_cast<const char *>(W);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kAmaxStages; ++st) asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(smem_addr(&mbar[st])));
+    asm volatile("fence.mbarrier_init.release.cluster;");
+    asm volatile("fence.proxy.async.shared::cta;");
+  }
+  __syncthreads();
+  pdl_wait();  // W may be written by the previous kernel of the stream
+  pdl_launch_dependents();
+  auto bytes_of = [&](int64_t ch) { return (uint32_t)(min(kUnits, n16 - ch * kUnits) * 16); };
+  auto issue = [&](int64_t ch, int st) {
+    const uint32_t mb = smem_addr(&mbar[st]), nb = bytes_of(ch);
+    asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(mb), "r"(nb) : "memory");
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(stage + (int64_t)st * kUnits)), "l"(src + ch * kAmaxChunk), "r"(nb), "r"(mb)
+                 : "memory");
+  };
+  if (threadIdx.x == 0)
+    for (int st = 0; st < kAmaxStages; ++st) {
+      const int64_t ch = blockIdx.x + (int64_t)st * gridDim.x;
+      if (ch < nch) issue(ch, st);
+    }
+  uint32_t m = 0u;
+  bool ok = true;  // uniform over the CTA
+  int j = 0;
+  for (int64_t ch = blockIdx.x; ch < nch; ch += gridDim.x, ++j) {
+    const int st = j % kAmaxStages;
+    const bool arrived = mbar_wait_bounded(smem_addr(&mbar[st]), (uint32_t)((j / kAmaxStages) & 1));
+    if (!__syncthreads_and(arrived)) {
+      ok = false;
+      break;
+    }
+    const uint4 *p = stage + (int64_t)st * kUnits;
+    const int units = (int)(bytes_of(ch) / 16);
+    for (int i = threadIdx.x; i < units; i += kThreads) {
+      const uint4 v = p[i];
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.x));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.y));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.z));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.w));
+    }
+    __syncthreads();  // the stage has been read by every thread
+    if (threadIdx.x == 0) {
+      const int64_t nx = ch + (int64_t)kAmaxStages * gridDim.x;
+      if (nx < nch) issue(nx, st);
+    }
+  }
+  if (!ok) {  // a copy did not arrive in time: wait (bounded) for every copy still in flight
+    if (threadIdx.x == 0)
+      for (int jj = j; jj < j + kAmaxStages; ++jj) {
+        if ((int64_t)blockIdx.x + (int64_t)jj * gridDim.x >= nch) break;
+        mbar_wait_bounded(smem_addr(&mbar[jj % kAmaxStages]), (uint32_t)((jj / kAmaxStages) & 1));
+      }
+    if (threadIdx.x == 0) part[blockIdx.x] = 0xFFFFFFFFu;
+    return;
+  }
+  m &= 0x7FFF7FFFu;
+  m = block_max_u32(max(m & 0xFFFFu, m >> 16), red);
+  if (threadIdx.x == 0) part[blockIdx.x] = m;
+}
+
 // ---------------------------------------------------------------------------
 // a2-a4, a7: max rule and FourOverSix
 // ---------------------------------------------------------------------------
@@ -707,6 +798,19 @@ cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int
   return cudaLaunchKernelEx(&cfg, k_amax_partials, static_cast<const uint4 *>(W), n16, part);
 }
 
+cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = make_cfg(grid, st);
+  cfg.dynamicSmemBytes = kAmaxBulkSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_amax_bulk, static_cast<const uint4 *>(W), n16, part);
+}
+
+int amax_bulk_chunks(int64_t n16) { return (int)((n16 * 16 + kAmaxChunk - 1) / kAmaxChunk); }
+
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
                                  cudaStream_t st) {
@@ -782,7 +886,10 @@ cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *ama
 }
 
 cudaError_t prepare_decoupled_kernel() {
-  return cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
+  cudaError_t e = cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_amax_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAmaxBulkSmem);
+  return e;
 }
 
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out,
@@ -815,13 +922,14 @@ int max_active_ctas(int which) {
   int n = 0;
   cudaError_t e = cudaSuccess;
   switch (which) {
-    case kKernAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
+    case kKernAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_bulk, kThreads, kAmaxBulkSmem); break;
     case kKernQuantMax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeMax>, kThreads, 0); break;
     case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
     case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
     case kKernDecoupled:
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kDecThreads, kDecTableBytes);
       break;
+    case kKernAmaxLdg: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
     case kKernGroupAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_amax, kThreads, 0); break;
     case kKernGroupQuantMax:
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_quant<kModeMax>, kThreads, 0);

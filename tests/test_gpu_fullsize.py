@@ -95,3 +95,15 @@ def test_llama3_8b_tensors(index):
     w = synthetic.llama3_8b_tensor(index)
     check_full(w, oracle.FOUR_OVER_SIX, 0)
     check_sampled(w, oracle.CJSO_DECOUPLED, 5, nsample=3000)
+
+
+@pytest.mark.parametrize("mode,iters", [(oracle.MAX, 0), (oracle.FOUR_OVER_SIX, 0), (oracle.CJSO, 2)])
+def test_beyond_half_l2_with_a_partial_last_chunk(mode, iters):
+    """4099 x 9232 (72 MiB of bf16, more than half of L2): the amax pass streams
+    W through shared memory in 32 KiB bulk copies, the last one partial."""
+    w = synthetic.student_t(4099, 9232, 4.0, 0.02, 4242)
+    assert (w.nbytes % 32768) != 0
+    if mode == oracle.CJSO:
+        check_sampled(w, mode, iters)
+    else:
+        check_full(w, mode, iters)
