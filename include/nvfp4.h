@@ -90,7 +90,10 @@ enum nvfp4_mode {
  *   alpha  device, 4-byte aligned, 1 float (written; 0 for an empty or all-zero W).
  *   stream cudaStream_t.
  * Returns an nvfp4_status.  rows*cols == 0 is valid: only *alpha = 0 is written
- * (W, codes and scales may then be NULL).
+ * (W, codes and scales may then be NULL).  Every wait inside a kernel is
+ * bounded: should a device-side copy never complete, the kernel gives up
+ * after its limit and *alpha comes out NaN (the status, returned before the
+ * kernels run, cannot report it).
  */
 int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iters,
                    uint8_t *codes, uint8_t *scales, float *alpha, cudaStream_t stream);
