@@ -260,9 +260,11 @@ def run_ours(args, modes):
     W_host = torch.from_numpy(w_bits.view(np.int16)).view(torch.bfloat16)
     Wd = [W_host.to(dev) for _ in range(ncopy)]
     mids = [MODE_IDS[m] for m in modes]
-    outs = {m: (torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
-                torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
-                torch.empty(1, dtype=torch.float32, device=dev)) for m in mids if m < 4}
+    # outputs rotate with the inputs (one set per copy and mode), so they are
+    # written back to HBM as a real sequence of tensors would be
+    outs = {m: [(torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
+                 torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
+                 torch.empty(1, dtype=torch.float32, device=dev)) for _ in range(ncopy)] for m in mids if m < 4}
 
     if any(m >= 4 for m in mids):  # consumer inputs: this tensor quantized (max rule) once per rotation slot
         dq_in = []
@@ -289,7 +291,7 @@ def run_ours(args, modes):
             st = nv.nvfp4_dequantize(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, dq_out[i].data_ptr(),
                                      s.cuda_stream)
         else:
-            c, sc, a = outs[mode]
+            c, sc, a = outs[mode][next(k for k in range(ncopy) if Wd[k] is w)]
             st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
                                    a.data_ptr(), s.cuda_stream)
         if st != 0:
@@ -369,7 +371,8 @@ def run_ours(args, modes):
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
            "config": {"workload": args.workload, "desc": desc, "rows": rows, "cols": cols, "modes": list(modes),
                       "cjso_iters": args.iters if any(m >= 2 for m in mids) else None,
-                      "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB)",
+                      "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB) "
+                            f"and {ncopy} output sets per mode",
                       "launch": launch, "parallelism": f"{ws} independent replica(s), one tensor per rank"},
            "gpu_launches": sum(kernels_per_call(m, args.iters) for m in mids) * args.steps, "clocks": csum}
     if args.quick:
@@ -458,8 +461,8 @@ def run_ours(args, modes):
     qmids = [m for m in mids if m < 4]
     slots = []
     for _ in range(2):
-        o = {m: tuple(torch.empty_like(t) for t in outs[m]) for m in qmids}
-        ho = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m]) for m in qmids}
+        o = {m: tuple(torch.empty_like(t) for t in outs[m][0]) for m in qmids}
+        ho = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m][0]) for m in qmids}
         slots.append({"W": torch.empty_like(Wd[0]), "outs": o, "host": ho,
                       "h2d": torch.cuda.Event(), "comp": torch.cuda.Event(), "d2h": torch.cuda.Event()})
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
