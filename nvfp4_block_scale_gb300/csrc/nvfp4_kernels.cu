@@ -131,17 +131,26 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
   uint32_t m = 0u;
   for (int64_t base = (int64_t)blockIdx.x * tile + threadIdx.x; base < n16; base += (int64_t)gridDim.x * tile) {
     uint4 v[kAmaxUnroll];
+    if (base + (int64_t)(kAmaxUnroll - 1) * kThreads < n16) {
+      // whole tile: every load issued before the first use (volatile keeps the order)
 #pragma unroll
-    for (int u = 0; u < kAmaxUnroll; ++u) {
-      const int64_t i = base + (int64_t)u * kThreads;
-      v[u] = i < n16 ? __ldg(W + i) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < kAmaxUnroll; ++u)
+        asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                     : "l"(W + base + (int64_t)u * kThreads));
+    } else {
+#pragma unroll
+      for (int u = 0; u < kAmaxUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kThreads;
+        v[u] = i < n16 ? __ldg(W + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kAmaxUnroll; ++u) {
-      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].x));
-      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].y));
-      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].z));
-      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].w));
+      asm volatile("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].x));
+      asm volatile("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].y));
+      asm volatile("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].z));
+      asm volatile("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v[u].w));
     }
   }
   m &= 0x7FFF7FFFu;
