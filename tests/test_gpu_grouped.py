@@ -91,3 +91,12 @@ def test_grouped_one_large_tensor_beyond_l2():
     rc, rs, ra = nv.quantize(W, nv.FOUR_OVER_SIX)
     torch.cuda.synchronize()
     assert torch.equal(c, rc) and torch.equal(s, rs) and a.item() == ra.item()
+
+
+def test_grouped_all_empty_and_zero_count():
+    Wd = [torch.empty((0, 16), dtype=torch.bfloat16, device="cuda"),
+          torch.empty((3, 0), dtype=torch.bfloat16, device="cuda")]
+    outs = nv.quantize_grouped(Wd, nv.FOUR_OVER_SIX)
+    torch.cuda.synchronize()
+    assert all(a.item() == 0.0 for _, _, a in outs)
+    assert nv.nvfp4_quantize_grouped(None, 0, 0, 0, torch.cuda.current_stream().cuda_stream) == 0
