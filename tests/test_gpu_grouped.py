@@ -100,3 +100,17 @@ def test_grouped_all_empty_and_zero_count():
     torch.cuda.synchronize()
     assert all(a.item() == 0.0 for _, _, a in outs)
     assert nv.nvfp4_quantize_grouped(None, 0, 0, 0, torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_grouped_full_llama3_stack_matches_single_calls():
+    """The benchmark's launch configuration: all 224 tensors of the
+    Llama-3-8B-shaped stack (13 GiB, generated on the device as the benchmark
+    does) in one grouped FourOverSix call, every tensor bit-identical to its
+    single-tensor call (which the other tests check against the oracle)."""
+    import bench
+    shapes, Ws = bench.model_tensors(torch.device("cuda"))
+    outs = nv.quantize_grouped(Ws, nv.FOUR_OVER_SIX)
+    for W, (c, s, a) in zip(Ws, outs):
+        rc, rs, ra = nv.quantize(W, nv.FOUR_OVER_SIX)
+        assert torch.equal(c, rc) and torch.equal(s, rs) and a.item() == ra.item()
+        del rc, rs, ra
