@@ -131,3 +131,14 @@ def test_swizzled_size_and_checks():
     assert nv.nvfp4_swizzle_scales(A16, 4, 17, A16, None) == INVALID
     assert nv.nvfp4_swizzle_scales(None, 4, 16, A16, None) == INVALID
     assert nv.nvfp4_swizzle_scales(A16, 4, 16, A16 + 2, None) == MISALIGNED
+
+
+def test_profiler_api_without_launches():
+    assert nv.nvfp4_profiler_reset() == OK
+    assert nv.nvfp4_profiler_enable(1) == OK
+    assert nv.nvfp4_profiler_enable(0) == OK
+    assert nv.nvfp4_profiler_kinds() == 0
+    name = ctypes.create_string_buffer(64)
+    launches, total = ctypes.c_int64(), ctypes.c_double()
+    assert nv.nvfp4_profiler_get(0, name, 64, ctypes.byref(launches), ctypes.byref(total)) == INVALID
+    assert nv.profiler_report() == {}
