@@ -202,7 +202,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   // (measured faster there), plain 16-byte loads for smaller ones (faster there)
   const bool bulk = 2 * n > int64_t(d->l2) / 2;
   const int g_amax = bulk ? (int)std::min<int64_t>(amax_bulk_chunks(H), int64_t(d->sms) * d->occ[kKernAmax])
-                          : grid_for(*d, kKernAmaxLdg, H / 16 + 1);  // 16 loads per thread per tile
+                          : grid_for(*d, kKernAmaxLdg, H / 8 + 1);  // 8 loads per thread per tile
   const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);

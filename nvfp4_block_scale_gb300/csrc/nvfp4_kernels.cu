@@ -120,7 +120,7 @@ __device__ __forceinline__ uint4 load_half(const uint4 *__restrict__ W, int64_t 
 // the stream, it waits for that grid before touching W, then lets the
 // quantize kernel be scheduled at once; that kernel waits for this grid's
 // completion before reading the partials.
-constexpr int kAmaxUnroll = 16;
+constexpr int kAmaxUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restrict__ W, int64_t n16,
                                                             uint32_t *__restrict__ part) {
