@@ -66,6 +66,7 @@ WORKLOADS = {
                 ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant", "gemv", "swizzle")),
 }
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy bandwidth is the roofline)
 ONE_PASS = 2.5625   # B/elem: W read once (2) + codes (0.5) + scales (1/16)
 TWO_PASS = 4.5625   # B/elem: W read twice (alpha needs the global max first)
 DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P FMA 2 + R FMA 2)
@@ -436,14 +437,15 @@ def run_ours(args, modes):
         per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "us_per_call": call_ms * 1e3,
                           "us_isolated_call": times[1] * 1e3,
                           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over},
+                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
+                                       "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
                           "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
                                                       for kn, (c, t) in rep.items()}}
     heavy = max(per_mode, key=lambda k: per_mode[k]["us_per_call"])
     hr = per_mode[heavy]["roofline"]
     out["per_mode"] = per_mode
     out["roofline"] = {"bound": hr["bound"], "achieved": hr["achieved"], "peak": hr["peak"], "unit": hr["unit"],
-                       "frac": hr["frac"],
+                       "frac": hr["frac"], "frac_of_nominal": hr["frac_of_nominal"],
                        "traffic": recorded_traffic(f"nvfp4_quantize({heavy})@{args.workload}"),
                        "kernel": (f"nvfp4_quantize({heavy}) = "
                                   + " + ".join(per_mode[heavy]["kernels_event_bracketed"])
@@ -662,7 +664,8 @@ def run_model(args, modes):
         per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "ms_per_call": call_ms,
                           "per_tensor_calls_ms": per_tensor_ms,
                           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over},
+                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
+                                       "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
                           "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
                                                       for kn, (c, t) in rep.items()}}
     heavy = max(per_mode, key=lambda x: per_mode[x]["ms_per_call"])
