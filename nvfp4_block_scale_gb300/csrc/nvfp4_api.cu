@@ -207,7 +207,22 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
   const int64_t dec_full = int64_t(d->sms) * d->occ[kKernDecoupled];  // 1024-thread CTAs
-  const int g_dec = (int)((B + 1023) / 1024 < dec_full ? (B + 1023) / 1024 : dec_full);
+  // decoupled search: 1, 2 or 4 lanes per block, whichever finishes first in
+  // candidate evaluations per thread (blocks per thread x candidates per lane)
+  int g_dec = 1, split_dec = 1;
+  {
+    int64_t best = INT64_MAX;
+    for (int sp = 1; sp <= 4; sp *= 2) {
+      const int64_t need = std::max<int64_t>(1, (B * sp + 1023) / 1024);
+      const int64_t grid = std::min(need, dec_full);
+      const int64_t cost = ((B * sp + grid * 1024 - 1) / (grid * 1024)) * ((101 + sp - 1) / sp);
+      if (cost < best) {
+        best = cost;
+        g_dec = (int)grid;
+        split_dec = sp;
+      }
+    }
+  }
 
   // scratch: amax partials | 2 x CJSO partial sums | alpha history
   const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);
@@ -244,7 +259,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
     }
     if (e == cudaSuccess && !plain) {
       TraceScope tr(kTrDecoupled, stream);
-      e = launch_decoupled(W, B, hist, T, scales, codes, g_dec, stream);
+      e = launch_decoupled(W, B, hist, T, scales, codes, g_dec, split_dec, stream);
     }
   }
   // The scratch goes back to the pool in stream order, after the last kernel.

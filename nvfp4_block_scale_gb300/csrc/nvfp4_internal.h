@@ -41,7 +41,7 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
                        uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                        int grid, cudaStream_t st);
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,
-                      int grid, cudaStream_t st);
+                             int grid, int split, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out, int grid,
                     cudaStream_t st);
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);

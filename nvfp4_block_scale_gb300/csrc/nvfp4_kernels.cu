@@ -461,14 +461,25 @@ __device__ __forceinline__ void bracket_e4m3(float dq, const float *ev_tab, uint
   hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
 }
 
+// SPLIT consecutive lanes share one block: lane `sub` of the group evaluates
+// k = sub, sub + SPLIT, ... in ascending order, keeping its first strict
+// minimum; the group then takes the least (g, 2k + h) over its lanes, which
+// is the first strict minimum over all 202 candidates in (k, lower-before-
+// upper) order.  SPLIT > 1 serves tensors with fewer blocks than the GPU has
+// threads.  Every lane of a warp runs the same number of iterations (lanes
+// past the last block idle inside), so the shuffles see the whole warp.
+template <int SPLIT>
 __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
                                                               const float *__restrict__ alpha_hist, int t,
                                                               uint8_t *__restrict__ scales,
                                                               uint32_t *__restrict__ codes32) {
   extern __shared__ float4 tab[];  // [code][k] = {sq, rq, sd_lo, sd_hi}
   __shared__ float ev_tab[128], m_tab[kDecK];
-  const int64_t stride = (int64_t)gridDim.x * kDecThreads;
-  int64_t b = (int64_t)blockIdx.x * kDecThreads + threadIdx.x;
+  const int sub = threadIdx.x % SPLIT;
+  const int64_t per_cta = kDecThreads / SPLIT;  // blocks per CTA and iteration
+  const int64_t stride = (int64_t)gridDim.x * per_cta;
+  const int64_t warp_first = ((int64_t)blockIdx.x * kDecThreads + (threadIdx.x & ~31)) / SPLIT;
+  int64_t b = ((int64_t)blockIdx.x * kDecThreads + threadIdx.x) / SPLIT;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
   if (threadIdx.x < 128) ev_tab[threadIdx.x] = e4m3_value(threadIdx.x);
@@ -489,40 +500,53 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   }
   __syncthreads();
 
-  for (; b < B; b += stride) {
+  for (int64_t wf = warp_first; wf < B; wf += stride, b += stride) {  // wf: the warp's first block
+    const bool live = b < B;
     const int64_t nb = b + stride;
     const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
-    const uint32_t d0 = scales[b];
-    uint32_t best_d = d0, c0, c1;
-    float P, R;
-    if (__fmul_rn(alpha, ev_tab[d0]) != 0.0f) {
+    const uint32_t d0 = live ? scales[b] : 0u;
+    const bool search = live && __fmul_rn(alpha, ev_tab[d0]) != 0.0f;
+    float best_g = __int_as_float(0x7F800000);  // +inf
+    int best_i = 2 * kDecK;                      // candidate index 2k + h
+    if (search) {
       BlockH16 bh;
       make_h16(blk, am, bh);
       const float4 *row = tab + d0 * kDecK;
-      float best_g = __int_as_float(0x7F800000);  // +inf
-      int best_k = 0, best_h = 0;
-      for (int k = 0; k < kDecK; ++k) {
+      for (int k = sub; k < kDecK; k += SPLIT) {
         const float4 c = row[k];
-        float m2P;
+        float m2P, R;
         block_sums_h(blk, bh, c.x, c.y, m2P, R);
         const float glo = cand_err_m2p(c.z, m2P, R);
         const float ghi = cand_err_m2p(c.w, m2P, R);
-        if (glo < best_g) { best_g = glo; best_k = k; best_h = 0; }
-        if (ghi < best_g) { best_g = ghi; best_k = k; best_h = 1; }
+        if (glo < best_g) { best_g = glo; best_i = 2 * k; }
+        if (ghi < best_g) { best_g = ghi; best_i = 2 * k + 1; }
       }
-      const float4 c = row[best_k];
-      quant16<false>(blk, c.x, c.y, c0, c1, P, R);
-      uint32_t lo, hi;
-      bracket_e4m3(__fmul_rn(ev_tab[d0], m_tab[best_k]), ev_tab, lo, hi);
-      best_d = best_h ? hi : lo;
-    } else {
-      quant16<false>(blk, 0.0f, 0.0f, c0, c1, P, R);  // zero scale: sign-only codes
     }
-    codes32[2 * b] = c0;
-    codes32[2 * b + 1] = c1;
-    scales[b] = (uint8_t)best_d;
+#pragma unroll
+    for (int o = 1; o < SPLIT; o <<= 1) {  // least (g, index) over the group's lanes
+      const float g2 = __shfl_xor_sync(0xFFFFFFFFu, best_g, o);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, best_i, o);
+      if (g2 < best_g || (g2 == best_g && i2 < best_i)) { best_g = g2; best_i = i2; }
+    }
+    if (live && sub == 0) {
+      uint32_t best_d = d0, c0, c1;
+      float P, R;
+      if (search) {
+        const int best_k = best_i >> 1;
+        const float4 c = tab[d0 * kDecK + best_k];
+        quant16<false>(blk, c.x, c.y, c0, c1, P, R);
+        uint32_t lo, hi;
+        bracket_e4m3(__fmul_rn(ev_tab[d0], m_tab[best_k]), ev_tab, lo, hi);
+        best_d = (best_i & 1) ? hi : lo;
+      } else {
+        quant16<false>(blk, 0.0f, 0.0f, c0, c1, P, R);  // zero scale: sign-only codes
+      }
+      codes32[2 * b] = c0;
+      codes32[2 * b + 1] = c1;
+      scales[b] = (uint8_t)best_d;
+    }
     a0 = n0;
     a1 = n1;
   }
@@ -860,7 +884,7 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
 }
 
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
-                             uint8_t *codes, int grid, cudaStream_t st) {
+                             uint8_t *codes, int grid, int split, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = kDecTableBytes;
@@ -869,8 +893,11 @@ cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decoupled, static_cast<const uint4 *>(W), B, alpha_hist, t, scales,
-                            reinterpret_cast<uint32_t *>(codes));
+  const uint4 *w = static_cast<const uint4 *>(W);
+  uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  if (split == 4) return cudaLaunchKernelEx(&cfg, k_decoupled<4>, w, B, alpha_hist, t, scales, c);
+  if (split == 2) return cudaLaunchKernelEx(&cfg, k_decoupled<2>, w, B, alpha_hist, t, scales, c);
+  return cudaLaunchKernelEx(&cfg, k_decoupled<1>, w, B, alpha_hist, t, scales, c);
 }
 
 cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st) {
@@ -895,7 +922,11 @@ cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *ama
 }
 
 cudaError_t prepare_decoupled_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
+  cudaError_t e = cudaFuncSetAttribute(k_decoupled<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_decoupled<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_decoupled<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_amax_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAmaxBulkSmem);
   return e;
@@ -936,7 +967,7 @@ int max_active_ctas(int which) {
     case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
     case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
     case kKernDecoupled:
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled, kDecThreads, kDecTableBytes);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled<1>, kDecThreads, kDecTableBytes);
       break;
     case kKernAmaxLdg: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
     case kKernGroupAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_amax, kThreads, 0); break;
