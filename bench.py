@@ -217,7 +217,7 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=2.0, max_rows=None):
+def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=10.0, max_rows=None):
     """The oracle as it stands on all host cores; the first `max_rows` rows."""
     import oracle
     threads = os.cpu_count() or 1
