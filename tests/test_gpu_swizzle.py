@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 E2M1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (128, 64), (300, 160), (129, 2064), (4096, 4096)])
+@pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (128, 64), (300, 160), (129, 2064), (4096, 4096),
+                                       (8192, 28672)])  # the last: the benchmark's 8192x28672 tensor
 def test_swizzle_matches_oracle(rows, cols):
     rng = np.random.default_rng(rows * 31 + cols)
     sc = rng.integers(0, 127, (rows, cols // 16)).astype(np.uint8)
