@@ -84,7 +84,7 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W <= L2/2: one HBM read' if fits else 'W read twice'})"
     if mode == 4:  # dequantize: codes + scales in, bf16 out
         return "hbm", "GB/s", ONE_PASS * n, "2.5625 B/elem (codes 0.5 + scales 1/16 read, bf16 2 written)"
-    if mode == 5:  # one-vector W4A16 product: codes + scales once, x and y negligible
+    if mode == 5:  # W4A16 product: codes + scales once, x and y negligible
         return "hbm", "GB/s", 0.5625 * n, "0.5625 B/elem (codes + scales read once; + x, y)"
     if mode == 6:  # scale layout: scales read and written once
         return "hbm", "GB/s", 0.125 * n, "0.125 B/elem (scales read + written)"
@@ -273,8 +273,8 @@ def run_ours(args, modes):
             c, sc, a = nv.quantize(Wd[i], nv.MAX)
             dq_in.append((c, sc, a))
         dq_out = [torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) for _ in range(ncopy)]
-        gx = torch.randn((1, cols), device=dev).to(torch.bfloat16)
-        gy = torch.empty((1, rows), dtype=torch.float32, device=dev)
+        gx = torch.randn((args.gemv_batch, cols), device=dev).to(torch.bfloat16)
+        gy = torch.empty((args.gemv_batch, rows), dtype=torch.float32, device=dev)
         gz = torch.empty(nv.nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=dev)
 
     def call(mode, w, s):
@@ -284,7 +284,7 @@ def run_ours(args, modes):
         elif mode == 5:  # one-vector product with the slot's quantized tensor
             i = next(k for k in range(ncopy) if Wd[k] is w)
             c, sc, a = dq_in[i]
-            st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), 1,
+            st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.gemv_batch,
                                gy.data_ptr(), s.cuda_stream)
         elif mode == 4:  # dequantize the slot of this W into that slot's output
             i = next(k for k in range(ncopy) if Wd[k] is w)
@@ -371,7 +371,8 @@ def run_ours(args, modes):
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
            "config": {"workload": args.workload, "desc": desc, "rows": rows, "cols": cols, "modes": list(modes),
-                      "cjso_iters": args.iters if any(m >= 2 for m in mids) else None,
+                      "cjso_iters": args.iters if any(2 <= m <= 3 for m in mids) else None,
+                      "gemv_batch": args.gemv_batch if 5 in mids else None,
                       "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB) "
                             f"and {ncopy} output sets per mode",
                       "launch": launch, "parallelism": f"{ws} independent replica(s), one tensor per rank"},
@@ -758,6 +759,7 @@ def main():
     ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
     ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
     ap.add_argument("--layers", type=int, default=32, help=f"layers of the {MODEL} stack (1..32)")
+    ap.add_argument("--gemv-batch", type=int, default=1, help="activation vectors of the gemv mode (1..8)")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
