@@ -179,3 +179,16 @@ def test_bf16_round_matches_torch():
     ours = oracle.bf16_round(v)
     ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(ours, ref)
+
+
+@pytest.mark.parametrize("lo,hi", [(0.5, 2.0), (256.0, 464.0)])
+def test_e4m3_exhaustive_normal_binades(lo, hi):
+    """Every fp32 bit pattern of two normal binades and of the top binade up
+    to the overflow point: the oracle's E4M3 rounding equals PyTorch's
+    float8_e4m3fn cast (the subnormal range has its own exhaustive test; every
+    binade's decision points are in the structured test)."""
+    b_lo, b_hi = int(np.float32(lo).view(np.uint32)), int(np.float32(hi).view(np.uint32))
+    step = 1 << 22
+    for b0 in range(b_lo, b_hi, step):
+        v = f32_from_bits(np.arange(b0, min(b0 + step, b_hi), dtype=np.uint32))
+        assert np.array_equal(oracle.e4m3_encode(v), torch_e4m3(v)), hex(b0)
