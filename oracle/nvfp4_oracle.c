@@ -29,7 +29,7 @@
  *             Delta^q scaled by [0.5, 1.5] in steps of 0.01; Delta^d limited to
  *             the two nearest E4M3 values; keep the pair of least error.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1  block = 16 consecutive elements of one row (row-major [rows, cols]).
  *   R2  E2M1 rounding ties go to the even code (round-half-even inside each
  *       piece of the [SOAR-Q] formula); magnitudes above 6 saturate to 6; the
