@@ -41,8 +41,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
 HEADLINE = "studentt_4k"
-MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5, "swizzle": 6}
-CONSUMERS = ("dequant", "gemv", "swizzle")  # modes that read a quantized tensor instead of producing one
+MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5, "swizzle": 6,
+            "gemm": 7}
+CONSUMERS = ("dequant", "gemv", "swizzle", "gemm")  # modes that read a quantized tensor instead of producing one
 
 
 def _synth():
@@ -73,10 +74,11 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1}[mode]
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1, 7: 2}[mode]
 
 
-def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
+def algorithmic(mode: int, iters: int, n: int, l2_bytes: int, batch: int = 1, hbm_gbs: float = 6660.0,
+                tc_tflops: float = 1884.6):
     """(bound, unit, algorithmic work of one call, rule) for a mode."""
     fits = 2 * n <= l2_bytes // 2
     if mode in (0, 1):
@@ -85,6 +87,11 @@ def algorithmic(mode: int, iters: int, n: int, l2_bytes: int):
     if mode == 4:  # dequantize: codes + scales in, bf16 out
         return "hbm", "GB/s", ONE_PASS * n, "2.5625 B/elem (codes 0.5 + scales 1/16 read, bf16 2 written)"
     if mode == 5:  # W4A16 product: codes + scales once, x and y negligible
+        return "hbm", "GB/s", 0.5625 * n, "0.5625 B/elem (codes + scales read once; + x, y)"
+    if mode == 7:  # tensor-core W4A16 product of `batch` vectors: HBM or bf16 tensor bound, whichever is longer
+        flops = 2.0 * n * batch
+        if flops / (tc_tflops * 1e12) > 0.5625 * n / (hbm_gbs * 1e9):
+            return "tensor", "TFLOP/s", flops, f"2 flop per weight and vector ({batch} vectors), bf16 tensor cores"
         return "hbm", "GB/s", 0.5625 * n, "0.5625 B/elem (codes + scales read once; + x, y)"
     if mode == 6:  # scale layout: scales read and written once
         return "hbm", "GB/s", 0.125 * n, "0.125 B/elem (scales read + written)"
@@ -168,6 +175,15 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor-core peak (burst: the product is timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def fp32_peak_tflops(sms: int, mhz: float) -> float:
@@ -273,18 +289,23 @@ def run_ours(args, modes):
             c, sc, a = nv.quantize(Wd[i], nv.MAX)
             dq_in.append((c, sc, a))
         dq_out = [torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) for _ in range(ncopy)]
-        gx = torch.randn((args.gemv_batch, cols), device=dev).to(torch.bfloat16)
-        gy = torch.empty((args.gemv_batch, rows), dtype=torch.float32, device=dev)
+        gx = torch.randn((args.batch, cols), device=dev).to(torch.bfloat16)
+        gy = torch.empty((args.batch, rows), dtype=torch.float32, device=dev)
         gz = torch.empty(nv.nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=dev)
 
     def call(mode, w, s):
         if mode == 6:  # the slot's scales into the tensor-core layout
             i = next(k for k in range(ncopy) if Wd[k] is w)
             st = nv.nvfp4_swizzle_scales(dq_in[i][1].data_ptr(), rows, cols, gz.data_ptr(), s.cuda_stream)
+        elif mode == 7:  # tensor-core product of `batch` vectors with the slot's quantized tensor
+            i = next(k for k in range(ncopy) if Wd[k] is w)
+            c, sc, a = dq_in[i]
+            st = nv.nvfp4_gemm(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.batch,
+                               gy.data_ptr(), s.cuda_stream)
         elif mode == 5:  # one-vector product with the slot's quantized tensor
             i = next(k for k in range(ncopy) if Wd[k] is w)
             c, sc, a = dq_in[i]
-            st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.gemv_batch,
+            st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.batch,
                                gy.data_ptr(), s.cuda_stream)
         elif mode == 4:  # dequantize the slot of this W into that slot's output
             i = next(k for k in range(ncopy) if Wd[k] is w)
@@ -372,7 +393,7 @@ def run_ours(args, modes):
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
            "config": {"workload": args.workload, "desc": desc, "rows": rows, "cols": cols, "modes": list(modes),
                       "cjso_iters": args.iters if any(2 <= m <= 3 for m in mids) else None,
-                      "gemv_batch": args.gemv_batch if 5 in mids else None,
+                      "batch": args.batch if (5 in mids or 7 in mids) else None,
                       "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB) "
                             f"and {ncopy} output sets per mode",
                       "launch": launch, "parallelism": f"{ws} independent replica(s), one tensor per rank"},
@@ -426,9 +447,13 @@ def run_ours(args, modes):
         torch.cuda.synchronize()
         nv.nvfp4_profiler_enable(0)
         rep = nv.profiler_report()
-        bound, unit, work, rule = algorithmic(m, args.iters, n, l2)
+        tc_peak, tc_kind = measured_bf16_tflops()
+        bound, unit, work, rule = algorithmic(m, args.iters, n, l2, args.batch, peak_hbm, tc_peak)
         if bound == "hbm":
             achieved, peak, pk = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind
+            over = "the whole call"
+        elif bound == "tensor":
+            achieved, peak, pk = work / (call_ms / 1e3) / 1e12, tc_peak, tc_kind
             over = "the whole call"
         else:  # the search kernel alone (its event-bracketed duration), not the CJSO sweeps before it
             kc, kt = rep["k_decoupled"]
@@ -759,7 +784,7 @@ def main():
     ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
     ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
     ap.add_argument("--layers", type=int, default=32, help=f"layers of the {MODEL} stack (1..32)")
-    ap.add_argument("--gemv-batch", type=int, default=1, help="activation vectors of the gemv mode (1..8)")
+    ap.add_argument("--batch", type=int, default=1, help="activation vectors of the gemv (1..8) and gemm (1..256) modes")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()

@@ -170,6 +170,21 @@ int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
                int64_t cols, const void *x, int batch, float *y, cudaStream_t stream);
 
 /*
+ * nvfp4_gemm -- the same product as nvfp4_gemv for 1..256 activation vectors,
+ *   on the tensor cores: the weights are dequantized (exactly as
+ *   nvfp4_dequantize writes them) into shared memory and multiplied with
+ *   bf16 x bf16 -> fp32 tcgen05 matrix multiplies; K is split over CTAs when
+ *   the row tiles alone would leave SMs idle, and the split partial sums are
+ *   added in a fixed order.  The tensor cores' fp32 accumulation order is the
+ *   hardware's; results repeat bit for bit for the same shapes.
+ * Arguments as for nvfp4_gemv, with batch in 1..256.  Scratch for the split
+ *   partial sums comes from the library's pool (4 * batch * rows * splits
+ *   bytes).  Should an internal wait time out, the affected outputs are NaN.
+ */
+int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
+               int64_t cols, const void *x, int batch, float *y, cudaStream_t stream);
+
+/*
  * nvfp4_swizzle_scales -- the E4M3 block scales of a quantized [rows, cols]
  *   tensor, from the linear [rows, cols/16] layout that nvfp4_quantize
  *   writes to the layout block-scaled tensor-core matrix multiplies read

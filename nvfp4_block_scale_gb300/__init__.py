@@ -60,6 +60,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_quantize_grouped.restype = ci
     L.nvfp4_gemv.argtypes = [vp, vp, vp, i64, i64, vp, ci, vp, vp]
     L.nvfp4_gemv.restype = ci
+    L.nvfp4_gemm.argtypes = [vp, vp, vp, i64, i64, vp, ci, vp, vp]
+    L.nvfp4_gemm.restype = ci
     L.nvfp4_swizzled_scales_bytes.argtypes = [i64, i64]
     L.nvfp4_swizzled_scales_bytes.restype = i64
     L.nvfp4_swizzle_scales.argtypes = [vp, i64, i64, vp, vp]
@@ -108,6 +110,10 @@ def nvfp4_dequantize(codes, scales, alpha, rows, cols, out, stream) -> int:
 
 def nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream) -> int:
     return load().nvfp4_gemv(codes, scales, alpha, rows, cols, x, batch, y, stream)
+
+
+def nvfp4_gemm(codes, scales, alpha, rows, cols, x, batch, y, stream) -> int:
+    return load().nvfp4_gemm(codes, scales, alpha, rows, cols, x, batch, y, stream)
 
 
 def nvfp4_swizzled_scales_bytes(rows, cols) -> int:
@@ -246,6 +252,20 @@ def gemv(codes, scales, alpha, rows: int, cols: int, x, out=None, stream=None):
     y = out if out is not None else torch.empty((batch, rows), dtype=torch.float32, device=x.device)
     _check(nvfp4_gemv(codes.data_ptr(), scales.data_ptr(), alpha.data_ptr(), rows, cols, x.data_ptr(), batch,
                       y.data_ptr(), _stream_ptr(stream)), "nvfp4_gemv")
+    return y
+
+
+def gemm(codes, scales, alpha, rows: int, cols: int, x, out=None, stream=None):
+    """As gemv, on the tensor cores, for x [batch, cols] with batch 1..256."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.shape[1] != cols:
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [batch, cols]")
+    batch = x.shape[0]
+    y = out if out is not None else torch.empty((batch, rows), dtype=torch.float32, device=x.device)
+    _check(nvfp4_gemm(codes.data_ptr(), scales.data_ptr(), alpha.data_ptr(), rows, cols, x.data_ptr(), batch,
+                      y.data_ptr(), _stream_ptr(stream)), "nvfp4_gemm")
     return y
 
 

@@ -74,6 +74,7 @@ int device_info(DevInfo **out) {
       if (e != cudaSuccess) return map_cuda(e);
       for (int k = 0; k < kKernCount; ++k) d.occ[k] = max_active_ctas(k);
       e = prepare_gemv_kernels();
+      if (e == cudaSuccess) e = prepare_gemm_tc_kernels();
       if (e != cudaSuccess) return map_cuda(e);
       cudaMemPoolProps props = {};
       props.allocType = cudaMemAllocationTypePinned;
@@ -115,12 +116,14 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------------------
 
 enum { kTrAmax = 0, kTrQuantMax, kTrQuantFos, kTrCjsoInit, kTrCjsoIter, kTrDecoupled, kTrDequant, kTrEncode,
-       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrSwizzle, kTrAmaxLdg, kTrKinds };
+       kTrGroupAmax, kTrGroupQuantMax, kTrGroupQuantFos, kTrGemv, kTrSwizzle, kTrAmaxLdg, kTrGemmTc,
+       kTrGemmTcReduce, kTrKinds };
 const char *const kTraceNames[kTrKinds] = {"k_amax_bulk",        "k_quant_max_fos<max>", "k_quant_max_fos<fos>",
                                            "k_cjso_sweep<init>",  "k_cjso_sweep<iter>",   "k_decoupled",
                                            "k_dequant",           "k_encode",             "k_group_amax",
                                            "k_group_quant<max>",  "k_group_quant<fos>",   "k_gemv",
-                                           "k_swizzle_scales",   "k_amax_partials"};
+                                           "k_swizzle_scales",   "k_amax_partials",      "k_gemm_tc",
+                                           "k_gemm_tc_reduce"};
 
 struct TraceRec {
   int kind;
@@ -367,6 +370,48 @@ int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   TraceScope tr(kTrGemv, stream);
   return map_cuda(launch_gemv(codes, scales, alpha, rows, cols, x, batch, y,
                               gemv_grid(d->sms, batch, rows, cols), stream));
+}
+
+int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows, int64_t cols,
+               const void *x, int batch, float *y, cudaStream_t stream) {
+  int st = check_shape(rows, cols);
+  if (st != NVFP4_OK) return st;
+  if (batch < 1 || batch > 256) return NVFP4_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  if (!alpha || (n > 0 && (!codes || !scales || !x || !y))) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(alpha, 4) || (n > 0 && (!aligned(codes, 8) || !aligned(x, 16) || !aligned(y, 4))))
+    return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  if (rows == 0) return NVFP4_OK;
+  if (cols == 0) return map_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(rows * batch), stream));
+  // split K so that every SM gets as many CTAs as fit (the K steps of one CTA
+  // run one after another), each over whole 64-column steps
+  const int64_t tiles = (rows + 127) / 128, ksteps = (cols + 63) / 64;
+  const int64_t want = int64_t(d->sms) * gemm_tc_ctas_per_sm(batch);
+  int64_t splits = std::max<int64_t>(1, std::min<int64_t>((want + tiles - 1) / tiles, ksteps));
+  const int64_t kspan = (ksteps + splits - 1) / splits * 64;
+  splits = (cols + kspan - 1) / kspan;  // every split has at least one step
+  if (splits == 1) {
+    TraceScope tr(kTrGemmTc, stream);
+    return map_cuda(launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, kspan, 1, y, stream));
+  }
+  const int64_t ny = int64_t(batch) * rows;
+  void *ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, sizeof(float) * (size_t)(ny * splits), d->pool, stream);
+  if (e != cudaSuccess) return map_cuda(e);
+  float *part = static_cast<float *>(ws);
+  {
+    TraceScope tr(kTrGemmTc, stream);
+    e = launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, kspan, (int)splits, part, stream);
+  }
+  if (e == cudaSuccess) {
+    TraceScope tr(kTrGemmTcReduce, stream);
+    e = launch_gemm_tc_reduce(part, (int)splits, ny, y, grid_for(*d, kKernDequant, ny), stream);
+  }
+  cudaError_t ef = cudaFreeAsync(ws, stream);
+  return map_cuda(e != cudaSuccess ? e : ef);
 }
 
 int64_t nvfp4_swizzled_scales_bytes(int64_t rows, int64_t cols) {

@@ -66,32 +66,6 @@ __device__ __forceinline__ void gemv_load(GemvLoad &L, const uint2 *__restrict__
     }
 }
 
-// 8 code bytes (16 weights) and their scale -> 8 bf16x2 of What: per byte,
-// the E2M1 pair -> f16x2 (exact) -> f32 pair, times s (one packed multiply,
-// fl(q * s)), -> bf16x2 (RNE).
-__device__ __forceinline__ void gemv_dequant(uint2 cw, float s, uint32_t (&w)[8]) {
-#pragma unroll
-  for (int k = 0; k < 8; k += 4) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
-        ".reg .f16 l0, u0, l1, u1, l2, u2, l3, u3;\n\t.reg .f32 fl0, fu0, fl1, fu1, fl2, fu2, fl3, fu3;\n\t"
-        ".reg .b64 p0, p1, p2, p3, ss;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 h0, b0;\n\tcvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 h2, b2;\n\tcvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
-        "mov.b32 {l0, u0}, h0;\n\tmov.b32 {l1, u1}, h1;\n\tmov.b32 {l2, u2}, h2;\n\tmov.b32 {l3, u3}, h3;\n\t"
-        "cvt.f32.f16 fl0, l0;\n\tcvt.f32.f16 fu0, u0;\n\tcvt.f32.f16 fl1, l1;\n\tcvt.f32.f16 fu1, u1;\n\t"
-        "cvt.f32.f16 fl2, l2;\n\tcvt.f32.f16 fu2, u2;\n\tcvt.f32.f16 fl3, l3;\n\tcvt.f32.f16 fu3, u3;\n\t"
-        "mov.b64 ss, {%5, %5};\n\t"
-        "mov.b64 p0, {fl0, fu0};\n\tmov.b64 p1, {fl1, fu1};\n\tmov.b64 p2, {fl2, fu2};\n\tmov.b64 p3, {fl3, fu3};\n\t"
-        "mul.rn.f32x2 p0, p0, ss;\n\tmul.rn.f32x2 p1, p1, ss;\n\tmul.rn.f32x2 p2, p2, ss;\n\tmul.rn.f32x2 p3, p3, ss;\n\t"
-        "mov.b64 {fl0, fu0}, p0;\n\tmov.b64 {fl1, fu1}, p1;\n\tmov.b64 {fl2, fu2}, p2;\n\tmov.b64 {fl3, fu3}, p3;\n\t"
-        "cvt.rn.bf16x2.f32 %0, fu0, fl0;\n\tcvt.rn.bf16x2.f32 %1, fu1, fl1;\n\t"
-        "cvt.rn.bf16x2.f32 %2, fu2, fl2;\n\tcvt.rn.bf16x2.f32 %3, fu3, fl3;\n\t}"
-        : "=r"(w[k]), "=r"(w[k + 1]), "=r"(w[k + 2]), "=r"(w[k + 3])
-        : "r"(k == 0 ? cw.x : cw.y), "f"(s));
-  }
-}
-
 // acc += sum over the 8 pairs of w * x (bf16 operands, fp32 accumulation).
 __device__ __forceinline__ float gemv_dot16(const uint32_t (&w)[8], const uint4 &xa, const uint4 &xb, float acc) {
   const uint32_t x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
@@ -172,7 +146,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const uint2 *__restrict__
 #pragma unroll
         for (int r = 0; r < kGemvRows; ++r) {
           uint32_t w[8];
-          gemv_dequant(cur.c[r][h], s_tab[cur.s[r][h]], w);
+          dequant16_bf16(cur.c[r][h], s_tab[cur.s[r][h]], w);
 #pragma unroll
           for (int b = 0; b < NB; ++b)
             acc[r][b] = gemv_dot16(w, xb[b * (kGemvChunk / 8) + j], xb[b * (kGemvChunk / 8) + j + 1], acc[r][b]);
@@ -240,7 +214,7 @@ __global__ void __launch_bounds__(kGemvResWarps * 32) k_gemv_resident(const uint
         const int64_t j = j0 + 32 * u;
         if (j < nblk) {
           uint32_t w[8];
-          gemv_dequant(c[u], s_tab[sc[u]], w);
+          dequant16_bf16(c[u], s_tab[sc[u]], w);
 #pragma unroll
           for (int b = 0; b < NB; ++b)
             acc[b] = gemv_dot16(w, xs_all[b * units + 2 * j], xs_all[b * units + 2 * j + 1], acc[b]);

@@ -142,3 +142,11 @@ def test_profiler_api_without_launches():
     launches, total = ctypes.c_int64(), ctypes.c_double()
     assert nv.nvfp4_profiler_get(0, name, 64, ctypes.byref(launches), ctypes.byref(total)) == INVALID
     assert nv.profiler_report() == {}
+
+
+def test_gemm_rejects_bad_arguments():
+    assert nv.nvfp4_gemm(A16, A16, A16, 4, 17, A16, 1, A16, None) == INVALID
+    assert nv.nvfp4_gemm(A16, A16, A16, 4, 16, A16, 0, A16, None) == INVALID
+    assert nv.nvfp4_gemm(A16, A16, A16, 4, 16, A16, 257, A16, None) == INVALID
+    assert nv.nvfp4_gemm(A16 + 4, A16, A16, 4, 16, A16, 1, A16, None) == MISALIGNED
+    assert nv.nvfp4_gemm(A16, A16, A16, 4, 16, A16 + 8, 1, A16, None) == MISALIGNED
