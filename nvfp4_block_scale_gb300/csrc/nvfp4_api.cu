@@ -386,12 +386,13 @@ int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   if (st != NVFP4_OK) return st;
   if (rows == 0) return NVFP4_OK;
   if (cols == 0) return map_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(rows * batch), stream));
-  // split K so that every SM gets as many CTAs as fit (the K steps of one CTA
-  // run one after another), each over whole 64-column steps
-  const int64_t tiles = (rows + 127) / 128, ksteps = (cols + 63) / 64;
-  const int64_t want = int64_t(d->sms) * gemm_tc_ctas_per_sm(batch);
+  // split K into about 8 CTAs per SM (the K steps of one CTA run one after
+  // another; measured best between 4 and 16 on the 8192x28672 tensor), each
+  // over whole 128-column steps
+  const int64_t tiles = (rows + 127) / 128, ksteps = (cols + 127) / 128;
+  const int64_t want = int64_t(d->sms) * 8;
   int64_t splits = std::max<int64_t>(1, std::min<int64_t>((want + tiles - 1) / tiles, ksteps));
-  const int64_t kspan = (ksteps + splits - 1) / splits * 64;
+  const int64_t kspan = (ksteps + splits - 1) / splits * 128;
   splits = (cols + kspan - 1) / kspan;  // every split has at least one step
   if (splits == 1) {
     TraceScope tr(kTrGemmTc, stream);

@@ -28,11 +28,15 @@
 
 namespace nvfp4 {
 
-constexpr int kTcThreads = 128;  // four warps: one TMEM lane quarter each
+constexpr int kTcThreads = 256;  // two threads per row of the tile; warps 0-3 read the accumulator back
 constexpr int kTcM = 128;
-constexpr int kTcK = 64;         // columns per step = one 128-byte swizzle row
+constexpr int kTcK = 128;        // columns per step = two 64-column (128-byte) swizzle atoms
 constexpr int kTcMaxN = 256;
-constexpr int kTcStages = 3;   // shared-memory stages of the A and X tiles
+// shared-memory stages of the A and X tiles: three while they fit twice per SM
+template <int N>
+struct TcStages {
+  static constexpr int value = N <= 64 ? 3 : 2;
+};
 constexpr long kTcSpin = 1L << 24;
 
 __device__ __forceinline__ uint32_t tc_smem(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -69,9 +73,9 @@ __device__ __forceinline__ bool tc_wait(uint32_t mbar, uint32_t parity) {
   return done != 0;
 }
 
-struct TcCodes {
-  uint2 c[4];
-  uint32_t s[4];
+struct TcCodes {  // this thread's 4 blocks of W for one step (32 code bytes and 4 scales)
+  uint4 c[2];
+  uint32_t s;
 };
 
 template <int N>
@@ -80,10 +84,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
                                                            const float *__restrict__ alpha_p, int64_t rows,
                                                            int64_t cols, const uint4 *__restrict__ x, int batch,
                                                            int64_t kspan, float *__restrict__ out) {
-  constexpr uint32_t kA = kTcM * 128u, kB = (uint32_t)N * 128u, kStage = kA + kB;
+  constexpr int S = TcStages<N>::value;
+  constexpr uint32_t kAtomA = kTcM * 128u, kAtomB = (uint32_t)N * 128u;  // one 64-column swizzle atom
+  constexpr uint32_t kA = 2 * kAtomA, kStage = kA + 2 * kAtomB;
   constexpr uint32_t kCols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;  // TMEM columns
   extern __shared__ uint8_t dsm[];
-  __shared__ __align__(8) uint64_t mbar[kTcStages];
+  __shared__ __align__(8) uint64_t mbar[S];
   __shared__ uint32_t tmem_slot;
   __shared__ float s_tab[256];
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -94,31 +100,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
   const int64_t k0 = (int64_t)blockIdx.y * kspan;
   const int64_t k1 = min(cols, k0 + kspan);
   const int nsteps = (int)((k1 - k0 + kTcK - 1) / kTcK);  // >= 1: the host sizes the splits so
-  const int64_t row = row0 + tid;
-  // this thread's row of W for a step: 4 blocks (8 code bytes and a scale each)
+  // adjacent threads take the two 64-column halves (swizzle atoms) of one row
+  const int trow = tid >> 1, half = tid & 1;
+  const int64_t row = row0 + trow;
+  const int64_t bpr = cols / 16;  // blocks per row
+  const bool vec = (cols % 64) == 0 && (reinterpret_cast<uintptr_t>(codes) % 16) == 0 &&
+                   (reinterpret_cast<uintptr_t>(scales) % 4) == 0;  // 4 blocks = two aligned 16-byte loads
+  const uint2 *crow = reinterpret_cast<const uint2 *>(codes) + (row < rows ? row : 0) * bpr;
+  const uint8_t *srow = scales + (row < rows ? row : 0) * bpr;
   auto load_codes = [&](int step, TcCodes &t) {
-    const int64_t c0 = k0 + (int64_t)step * kTcK;
+    const int64_t col0 = k0 + (int64_t)step * kTcK + 64 * half;
+    const int64_t b0 = col0 >> 4;
+    if (vec && step < nsteps && row < rows && col0 + 48 < k1) {  // all 4 blocks inside the range
+      t.c[0] = __ldg(reinterpret_cast<const uint4 *>(crow + b0));
+      t.c[1] = __ldg(reinterpret_cast<const uint4 *>(crow + b0) + 1);
+      t.s = __ldg(reinterpret_cast<const uint32_t *>(srow + b0));
+      return;
+    }
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u}, sc = 0u;  // zero code and scale: zero weights
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t col = c0 + 16 * j;
+      const int64_t col = col0 + 16 * j;
       if (step < nsteps && row < rows && col < k1) {
-        const int64_t blk = (row * cols + col) >> 4;
-        t.c[j] = __ldg(reinterpret_cast<const uint2 *>(codes) + blk);
-        t.s[j] = __ldg(scales + blk);
-      } else {
-        t.c[j] = make_uint2(0u, 0u);
-        t.s[j] = 0u;  // code 0: zero scale, zero weights
+        const uint2 v = __ldg(crow + (col >> 4));
+        w[2 * j] = v.x;
+        w[2 * j + 1] = v.y;
+        sc |= (uint32_t)__ldg(srow + (col >> 4)) << (8 * j);
       }
     }
+    t.c[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    t.c[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    t.s = sc;
   };
-  // the step's N x 64 tile of X into stage `st` (asynchronous 16-byte copies)
+  // the step's N x 128 tile of X into stage `st` (asynchronous 16-byte copies)
   auto issue_x = [&](int step, int st) {
     const int64_t c0 = k0 + (int64_t)step * kTcK;
     uint8_t *B = gbase + st * kStage + kA;
-    for (int u = tid; u < N * 8; u += kTcThreads) {
-      const int b = u >> 3, c = u & 7;
+    for (int u = tid; u < N * 16; u += kTcThreads) {
+      const int b = u >> 4, c = u & 15;
       const int64_t col = c0 + 8 * c;
-      uint8_t *dst = B + sw128((uint32_t)b, (uint32_t)c);
+      uint8_t *dst = B + (c >> 3) * kAtomB + sw128((uint32_t)b, (uint32_t)(c & 7));
       if (b < batch && col < k1)
         asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dst)),
                      "l"(x + ((int64_t)b * cols + col) / 8) : "memory");
@@ -132,15 +153,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
   load_codes(0, cur);
   load_codes(1, nx1);
   const float alpha = *alpha_p;
-  s_tab[tid] = __fmul_rn(alpha, e4m3_value(tid));
-  s_tab[tid + 128] = __fmul_rn(alpha, e4m3_value(tid + 128));
+  s_tab[tid] = __fmul_rn(alpha, e4m3_value(tid));  // kTcThreads == 256: every code
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(&tmem_slot)),
                  "r"(kCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int st = 0; st < kTcStages; ++st) asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(tc_smem(&mbar[st])));
+    for (int st = 0; st < S; ++st) asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(tc_smem(&mbar[st])));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   issue_x(0, 0);
@@ -151,37 +171,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
   const uint32_t idesc = tc_idesc(N);
   bool ok = true;  // uniform over the CTA
   for (int s = 0; s < nsteps; ++s) {
-    const int st = s % kTcStages;
-    const int sn = (s + 1) % kTcStages;
-    if (s >= 2) {  // stage sn was last read by the MMAs of step s - 2
-      const bool arrived = tc_wait(tc_smem(&mbar[sn]), (uint32_t)(((s - 2) / kTcStages) & 1));
+    const int st = s % S;
+    const int sn = (s + 1) % S;
+    if (s + 1 >= S) {  // stage sn was last read by the MMAs of step s + 1 - S
+      const int prev = s + 1 - S;
+      const bool arrived = tc_wait(tc_smem(&mbar[sn]), (uint32_t)((prev / S) & 1));
       if (!__syncthreads_and(arrived)) {
         ok = false;
         break;
       }
     }
-    if (s + 1 < nsteps) issue_x(s + 1, sn);
-    load_codes(s + 2, nx2);
-    uint8_t *A = gbase + st * kStage;
+    uint8_t *A = gbase + st * kStage + half * kAtomA;  // this thread's atom: columns 64*half ..
+    const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
+                            cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t w[8];
-      dequant16_bf16(cur.c[j], s_tab[cur.s[j]], w);
-      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)tid, 2u * j)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)tid, 2u * j + 1u)) = make_uint4(w[4], w[5], w[6], w[7]);
+      dequant16_bf16(make_uint2(cw[2 * j], cw[2 * j + 1]), s_tab[(cur.s >> (8 * j)) & 0xFFu], w);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, 2u * j)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, 2u * j + 1u)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    if (s + 1 < nsteps)  // this step's X has landed (the next step's may still be in flight)
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this step's X has landed
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
     __syncthreads();
+    // the next loads are issued after the proxy fence, which would otherwise wait for them
+    if (s + 1 < nsteps) issue_x(s + 1, sn);
+    load_codes(s + 2, nx2);
     if (tid == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;");
       const uint32_t a0 = base + st * kStage, b0 = a0 + kA;
 #pragma unroll
-      for (int kk = 0; kk < kTcK / 16; ++kk) {
-        const uint64_t ad = tc_desc(a0 + 32u * kk), bd = tc_desc(b0 + 32u * kk);
+      for (int kk = 0; kk < kTcK / 16; ++kk) {  // 4 K-slices of 16 in each of the two atoms
+        const uint32_t atom = (uint32_t)(kk >> 2), ko = 32u * (uint32_t)(kk & 3);
+        const uint64_t ad = tc_desc(a0 + atom * kAtomA + ko), bd = tc_desc(b0 + atom * kAtomB + ko);
         const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
         asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
@@ -196,14 +218,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
   asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the CTA
   if (ok) {  // the last commit covers every MMA of this CTA
     const int last = nsteps - 1;
-    ok = __syncthreads_and(tc_wait(tc_smem(&mbar[last % kTcStages]), (uint32_t)((last / kTcStages) & 1)));
+    ok = __syncthreads_and(tc_wait(tc_smem(&mbar[last % S]), (uint32_t)((last / S) & 1)));
   } else {   // give the MMAs already issued their time (bounded), then report NaN
-    for (int st = 0; st < kTcStages; ++st) tc_wait(tc_smem(&mbar[st]), 0u);
+    for (int st = 0; st < S; ++st) tc_wait(tc_smem(&mbar[st]), 0u);
   }
   asm volatile("tcgen05.fence::after_thread_sync;");
   float *dst = out + (int64_t)blockIdx.y * batch * rows;
+  const int64_t orow = row0 + tid;  // the row whose accumulator lane this thread reads (warps 0-3)
 #pragma unroll 1
-  for (int n0 = 0; n0 < N; n0 += 16) {
+  for (int n0 = 0; n0 < N && warp < 4; n0 += 16) {  // warp w reads tensor-memory lanes 32w..32w+31
     uint32_t r[16];
     const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)n0;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
@@ -213,10 +236,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__rest
                    "=r"(r[15])
                  : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (row < rows) {
+    if (orow < rows) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (n0 + i < batch) dst[(int64_t)(n0 + i) * rows + row] = ok ? __uint_as_float(r[i]) : __int_as_float(0x7FC00000);
+        if (n0 + i < batch) dst[(int64_t)(n0 + i) * rows + orow] = ok ? __uint_as_float(r[i]) : __int_as_float(0x7FC00000);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -236,7 +259,7 @@ __global__ void __launch_bounds__(256) k_gemm_tc_reduce(const float *__restrict_
 
 namespace {
 template <int N>
-size_t tc_smem_bytes() { return kTcStages * ((size_t)kTcM * 128 + (size_t)N * 128) + 1024; }
+size_t tc_smem_bytes() { return TcStages<N>::value * 2 * ((size_t)kTcM * 128 + (size_t)N * 128) + 1024; }
 
 template <int N>
 cudaError_t tc_launch(dim3 grid, const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
