@@ -392,6 +392,9 @@ int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   const int64_t tiles = (rows + 127) / 128, ksteps = (cols + 127) / 128;
   const int64_t want = int64_t(d->sms) * 8;
   int64_t splits = std::max<int64_t>(1, std::min<int64_t>((want + tiles - 1) / tiles, ksteps));
+  // the split partial sums (4 * batch * rows bytes each, written and read back)
+  // stay below the codes' own bytes (rows * cols / 2)
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, cols / (8 * int64_t(batch))));
   const int64_t kspan = (ksteps + splits - 1) / splits * 128;
   splits = (cols + kspan - 1) / kspan;  // every split has at least one step
   if (splits == 1) {
