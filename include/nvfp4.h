@@ -173,13 +173,15 @@ int nvfp4_gemv(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
  * nvfp4_gemm -- the same product as nvfp4_gemv for 1..256 activation vectors,
  *   on the tensor cores: the weights are dequantized (exactly as
  *   nvfp4_dequantize writes them) into shared memory and multiplied with
- *   bf16 x bf16 -> fp32 tcgen05 matrix multiplies; K is split over CTAs when
- *   the row tiles alone would leave SMs idle, and the split partial sums are
- *   added in a fixed order.  The tensor cores' fp32 accumulation order is the
- *   hardware's; results repeat bit for bit for the same shapes.
- * Arguments as for nvfp4_gemv, with batch in 1..256.  Scratch for the split
- *   partial sums comes from the library's pool (4 * batch * rows * splits
- *   bytes).  Should an internal wait time out, the affected outputs are NaN.
+ *   bf16 x bf16 -> fp32 tcgen05 matrix multiplies.  The work (128-row tiles
+ *   x 128-column steps) is cut into equal contiguous ranges, one per SM;
+ *   the partial sums of a tile shared by several ranges are added in range
+ *   order.  The tensor cores' fp32 accumulation order is the hardware's;
+ *   results repeat bit for bit for the same shapes on the same GPU model.
+ * Arguments as for nvfp4_gemv, with batch in 1..256.  Scratch for the
+ *   partial sums comes from the library's pool (at most about
+ *   4 * batch * 128 * (2 * rows / 128 + SMs) bytes).  Should an internal wait time out, the
+ *   affected outputs are NaN.
  */
 int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
                int64_t cols, const void *x, int batch, float *y, cudaStream_t stream);

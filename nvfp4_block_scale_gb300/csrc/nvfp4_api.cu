@@ -386,33 +386,20 @@ int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   if (st != NVFP4_OK) return st;
   if (rows == 0) return NVFP4_OK;
   if (cols == 0) return map_cuda(cudaMemsetAsync(y, 0, sizeof(float) * (size_t)(rows * batch), stream));
-  // split K into about 8 CTAs per SM (the K steps of one CTA run one after
-  // another; measured best between 4 and 16 on the 8192x28672 tensor), each
-  // over whole 128-column steps
-  const int64_t tiles = (rows + 127) / 128, ksteps = (cols + 127) / 128;
-  const int64_t want = int64_t(d->sms) * 8;
-  int64_t splits = std::max<int64_t>(1, std::min<int64_t>((want + tiles - 1) / tiles, ksteps));
-  // the split partial sums (4 * batch * rows bytes each, written and read back)
-  // stay below the codes' own bytes (rows * cols / 2)
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, cols / (8 * int64_t(batch))));
-  const int64_t kspan = (ksteps + splits - 1) / splits * 128;
-  splits = (cols + kspan - 1) / kspan;  // every split has at least one step
-  if (splits == 1) {
-    TraceScope tr(kTrGemmTc, stream);
-    return map_cuda(launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, kspan, 1, y, stream));
-  }
+  // one persistent CTA per SM over all (tile, 128-column step) pairs; the
+  // partial sums of tiles shared by several CTAs meet in a workspace
   const int64_t ny = int64_t(batch) * rows;
   void *ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, sizeof(float) * (size_t)(ny * splits), d->pool, stream);
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, gemm_tc_workspace_bytes(rows, cols, batch, d->sms), d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
   float *part = static_cast<float *>(ws);
   {
     TraceScope tr(kTrGemmTc, stream);
-    e = launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, kspan, (int)splits, part, stream);
+    e = launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, d->sms, part, y, stream);
   }
   if (e == cudaSuccess) {
     TraceScope tr(kTrGemmTcReduce, stream);
-    e = launch_gemm_tc_reduce(part, (int)splits, ny, y, grid_for(*d, kKernDequant, ny), stream);
+    e = launch_gemm_tc_reduce(part, rows, cols, batch, d->sms, y, grid_for(*d, kKernDequant, ny), stream);
   }
   cudaError_t ef = cudaFreeAsync(ws, stream);
   return map_cuda(e != cudaSuccess ? e : ef);

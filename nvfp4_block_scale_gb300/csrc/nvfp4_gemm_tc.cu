@@ -6,21 +6,36 @@
 //   [SOAR-DQ]  "SOAR: Scale Optimization for Accurate Reconstruction in NVFP4
 //              Quantization": dequantization equation.
 //
-// One CTA computes a 128-row x N tile of Y^T (N = the batch rounded up to 16)
-// over a range of K (split-K: partial sums go to a workspace and a second
-// kernel adds them in a fixed order).  Per K step of 64 columns:
-//   - the 128 threads dequantize one row of W each (4 blocks: 32 code bytes,
-//     4 scales) into a 128 x 64 bf16 tile and copy the N x 64 bf16 tile of X,
-//     both in shared memory in the K-major 128-byte-swizzled layout;
-//   - one thread issues four tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
-//     M = 128, K = 16 each) accumulating into tensor memory, and commits them
-//     to the stage's mbarrier, so the next step's dequantization overlaps them
-//     (two stages).
-// The 128 x N fp32 accumulator lives in tensor memory (one lane per row), is
-// read back with tcgen05.ld and written to the partial sums.  Every mbarrier
-// wait is bounded; a CTA that gives up writes NaN partials.
+// The work is a sequence of T = tiles x K steps: a step is 128 rows of W (one
+// tile) times 128 columns (K = ceil(cols / 128) steps per tile).  The grid is
+// persistent (at most one CTA per SM) and CTA c takes the contiguous range
+// [c T / G, (c+1) T / G) of that sequence, so every CTA gets the same number of
+// steps whatever the shape; where a range crosses a tile boundary the CTA
+// starts a new segment (a new accumulator).  Each segment's 128 x N partial
+// sum goes to a workspace slot and k_gemm_tc_reduce adds the slots of a tile
+// in CTA order (a fixed order: the result does not depend on timing).
+//
+// Roles inside a CTA (704 threads):
+//   - warps 0-15 (512 threads, four per row of the tile) dequantize.  Each
+//     thread keeps its own 16 code bytes per step (and every other thread
+//     the 4 scale bytes of itself and its neighbour) for the next D steps in
+//     flight in a shared-memory ring (cp.async), and per step writes its 32
+//     bf16 weights into the 128 x 128 A tile of the stage (K-major, 128-byte
+//     swizzle);
+//   - warp 16 (one lane) issues per step eight tcgen05.mma (kind::f16,
+//     bf16 x bf16 -> fp32, M = 128, K = 16 each) into a tensor-memory
+//     accumulator and commits them to the stage's mbarrier;
+//   - warp 17 (one lane) loads the N x 128 tile of X per step with TMA (the
+//     tensor map's 128-byte swizzle gives the layout the MMA reads) as soon as
+//     the stage's previous MMAs are done;
+//   - warps 18-21 read each finished accumulator back with tcgen05.ld (the
+//     accumulator is double-buffered, so this overlaps the next segment).
+// Every mbarrier wait is bounded; a CTA that gives up waits (bounded) for its
+// own copies and MMAs in flight, writes NaN to its workspace slots and frees
+// its tensor memory.
 #include <algorithm>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "nvfp4_device.cuh"
@@ -28,16 +43,38 @@
 
 namespace nvfp4 {
 
-constexpr int kTcThreads = 256;  // two threads per row of the tile; warps 0-3 read the accumulator back
-constexpr int kTcM = 128;
-constexpr int kTcK = 128;        // columns per step = two 64-column (128-byte) swizzle atoms
-constexpr int kTcMaxN = 256;
-// shared-memory stages of the A and X tiles: three while they fit twice per SM
+constexpr int kTcM = 128;            // rows per tile (tensor-memory lanes)
+constexpr int kTcK = 128;            // columns per step = two 64-column (128-byte) swizzle atoms
+constexpr int kTcProducers = 512;    // warps 0-15
+constexpr int kTcMmaWarp = 16;
+constexpr int kTcXWarp = 17;
+constexpr int kTcEpiWarp0 = 18;      // warps 18-21
+constexpr int kTcThreads = 704;
+constexpr uint32_t kTcSlot = 9216;   // ring slot: 512 x 16 B codes, 256 x 4 B scales
+constexpr int kTcDynBudget = 227 * 1024 - 2048;  // dynamic shared memory (static arrays take the rest)
+// A wait suspends the thread (no spinning) for up to kTcSuspendNs per try,
+// and gives up after kTcTries tries (about 2 s): far beyond any legitimate
+// wait, which lasts a few microseconds.
+constexpr uint32_t kTcSuspendNs = 1000000u;
+constexpr int kTcTries = 2000;
+
+// S stages, each a dequantized A tile (32 KiB) and the matching N x 128 tile
+// of X (N x 256 bytes), then D ring slots of codes (9 KiB each), within
+// 227 KiB.  A stage is freed by the completion of its MMAs.
 template <int N>
-struct TcStages {
-  static constexpr int value = N <= 64 ? 3 : 2;
+struct TcCfg {
+  static constexpr int S = N <= 32 ? 4 : N <= 128 ? 3 : 2;
+  static constexpr uint32_t kAtomA = kTcM * 128u;                  // one 64-column atom of A
+  static constexpr uint32_t kAtomB = (uint32_t)N * 128u;           // one 64-column atom of X
+  static constexpr uint32_t kStage = 2 * kAtomA + 2 * kAtomB;      // A atoms, then X atoms
+  static constexpr uint32_t kRing = S * kStage;                    // offset of the ring
+  static constexpr int D0 = (int)((kTcDynBudget - 1024 - (int)kRing) / (int)kTcSlot);
+  static constexpr int D = D0 > 12 ? 12 : D0;                       // ring depth (steps in flight)
+  static constexpr uint32_t kCols = N <= 32 ? 32u : (uint32_t)N;    // tensor-memory columns per accumulator
+  static constexpr size_t kSmem = 1024 + (size_t)kRing + (size_t)D * kTcSlot;
+  static_assert(D >= 3, "ring too shallow");
+  static_assert(kSmem <= (size_t)kTcDynBudget, "shared memory");
 };
-constexpr long kTcSpin = 1L << 24;
 
 __device__ __forceinline__ uint32_t tc_smem(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -65,263 +102,420 @@ __device__ __forceinline__ uint32_t tc_idesc(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 }
 
-__device__ __forceinline__ bool tc_wait(uint32_t mbar, uint32_t parity) {
-  uint32_t done = 0;
-  for (long it = 0; !done && it < kTcSpin; ++it)
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t mb, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mb), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mb) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mb) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mb, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t mb, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(mb), "r"(parity), "n"(kTcSuspendNs) : "memory");
   return done != 0;
 }
 
-struct TcCodes {  // this thread's 4 blocks of W for one step (32 code bytes and 4 scales)
-  uint4 c[2];
-  uint32_t s;
+// Bounded wait for the phase of `parity`; gives up early once another role of
+// the CTA has raised `fail`, and raises it itself when the limit runs out.
+__device__ __forceinline__ bool tc_wait(uint32_t mb, uint32_t parity, volatile int *fail) {
+  for (int it = 0; it < kTcTries; ++it) {
+    if (mbar_try(mb, parity)) return true;
+    if (*fail) return false;
+  }
+  *fail = 1;
+  return false;
+}
+
+// The same wait without the early exit: used after a failure to let this
+// CTA's own copies and MMAs in flight finish before it leaves.
+__device__ __forceinline__ void tc_drain(uint32_t mb, uint32_t parity) {
+  for (int it = 0; it < kTcTries && !mbar_try(mb, parity); ++it) {
+  }
+}
+
+// Tiles of the work sequence: CTA c covers steps [c T / G, (c+1) T / G); the
+// CTA holding step g is floor(((g+1) G - 1) / T).
+__host__ __device__ __forceinline__ int64_t tc_first_step(int64_t c, int64_t T, int64_t G) { return c * T / G; }
+__host__ __device__ __forceinline__ int64_t tc_cta_of(int64_t g, int64_t T, int64_t G) { return ((g + 1) * G - 1) / T; }
+
+// Kernel arguments beside the tensor map.
+struct TcArgs {
+  const uint8_t *codes;
+  const uint8_t *scales;
+  const float *alpha;
+  int64_t rows, cols;
+  int batch;
+  int64_t K;      // steps per tile
+  int64_t T;      // steps in all
+  int maxc;       // workspace slots per tile
+  float *ws;      // [tiles][maxc][batch][128] partial sums
 };
 
 template <int N>
-__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const uint8_t *__restrict__ codes,
-                                                           const uint8_t *__restrict__ scales,
-                                                           const float *__restrict__ alpha_p, int64_t rows,
-                                                           int64_t cols, const uint4 *__restrict__ x, int batch,
-                                                           int64_t kspan, float *__restrict__ out) {
-  constexpr int S = TcStages<N>::value;
-  constexpr uint32_t kAtomA = kTcM * 128u, kAtomB = (uint32_t)N * 128u;  // one 64-column swizzle atom
-  constexpr uint32_t kA = 2 * kAtomA, kStage = kA + 2 * kAtomB;
-  constexpr uint32_t kCols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;  // TMEM columns
+__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap,
+                                                           const __grid_constant__ TcArgs a) {
+  using C = TcCfg<N>;
+  constexpr int S = C::S, D = C::D;
   extern __shared__ uint8_t dsm[];
-  __shared__ __align__(8) uint64_t mbar[S];
+  // full[s]: the stage's A tile written (one arrival per producer warp) and its
+  // X tile landed (one arrival with the TMA byte count); empty[s]: its MMAs done
+  __shared__ __align__(8) uint64_t full[S], empty[S], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_slot;
+  __shared__ int fail;
   __shared__ float s_tab[256];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t raw = tc_smem(dsm);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
   uint8_t *gbase = dsm + (base - raw);
-  const int64_t row0 = (int64_t)blockIdx.x * kTcM;
-  const int64_t k0 = (int64_t)blockIdx.y * kspan;
-  const int64_t k1 = min(cols, k0 + kspan);
-  const int nsteps = (int)((k1 - k0 + kTcK - 1) / kTcK);  // >= 1: the host sizes the splits so
-  // adjacent threads take the two 64-column halves (swizzle atoms) of one row
-  const int trow = tid >> 1, half = tid & 1;
-  const int64_t row = row0 + trow;
-  const int64_t bpr = cols / 16;  // blocks per row
-  const bool vec = (cols % 64) == 0 && (reinterpret_cast<uintptr_t>(codes) % 16) == 0 &&
-                   (reinterpret_cast<uintptr_t>(scales) % 4) == 0;  // 4 blocks = two aligned 16-byte loads
-  const uint2 *crow = reinterpret_cast<const uint2 *>(codes) + (row < rows ? row : 0) * bpr;
-  const uint8_t *srow = scales + (row < rows ? row : 0) * bpr;
-  auto load_codes = [&](int step, TcCodes &t) {
-    const int64_t col0 = k0 + (int64_t)step * kTcK + 64 * half;
-    const int64_t b0 = col0 >> 4;
-    if (vec && step < nsteps && row < rows && col0 + 48 < k1) {  // all 4 blocks inside the range
-      t.c[0] = __ldg(reinterpret_cast<const uint4 *>(crow + b0));
-      t.c[1] = __ldg(reinterpret_cast<const uint4 *>(crow + b0) + 1);
-      t.s = __ldg(reinterpret_cast<const uint32_t *>(srow + b0));
-      return;
-    }
-    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u}, sc = 0u;  // zero code and scale: zero weights
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t col = col0 + 16 * j;
-      if (step < nsteps && row < rows && col < k1) {
-        const uint2 v = __ldg(crow + (col >> 4));
-        w[2 * j] = v.x;
-        w[2 * j + 1] = v.y;
-        sc |= (uint32_t)__ldg(srow + (col >> 4)) << (8 * j);
-      }
-    }
-    t.c[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    t.c[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    t.s = sc;
-  };
-  // the step's N x 128 tile of X into stage `st` (asynchronous 16-byte copies)
-  auto issue_x = [&](int step, int st) {
-    const int64_t c0 = k0 + (int64_t)step * kTcK;
-    uint8_t *B = gbase + st * kStage + kA;
-    for (int u = tid; u < N * 16; u += kTcThreads) {
-      const int b = u >> 4, c = u & 15;
-      const int64_t col = c0 + 8 * c;
-      uint8_t *dst = B + (c >> 3) * kAtomB + sw128((uint32_t)b, (uint32_t)(c & 7));
-      if (b < batch && col < k1)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dst)),
-                     "l"(x + ((int64_t)b * cols + col) / 8) : "memory");
-      else
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
+  uint8_t *ring = gbase + C::kRing;
+  const int64_t G = gridDim.x;
+  const int64_t g0 = tc_first_step(blockIdx.x, a.T, G), g1 = tc_first_step(blockIdx.x + 1, a.T, G);
+  const int n = (int)(g1 - g0);  // >= 1: the host launches at most T CTAs
+  const int64_t t_first = g0 / a.K;
+  const int nseg = (int)((g1 - 1) / a.K - t_first + 1);
+  volatile int *vfail = &fail;
 
-  TcCodes cur, nx1, nx2;
-  load_codes(0, cur);
-  load_codes(1, nx1);
-  const float alpha = *alpha_p;
-  s_tab[tid] = __fmul_rn(alpha, e4m3_value(tid));  // kTcThreads == 256: every code
+  if (tid < 256) s_tab[tid] = __fmul_rn(*a.alpha, e4m3_value(tid));
+  if (tid == 0) fail = 0;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem(&tmem_slot)),
-                 "r"(kCols));
+                 "r"(2 * C::kCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (tid == 0) {
-    for (int st = 0; st < S; ++st) asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(tc_smem(&mbar[st])));
-    asm volatile("fence.mbarrier_init.release.cluster;");
+  if (tid == kTcMmaWarp * 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(tc_smem(&full[s]), kTcProducers / 32 + 1);
+      mbar_init(tc_smem(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tc_smem(&acc_full[b]), 1);
+      mbar_init(tc_smem(&acc_empty[b]), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  issue_x(0, 0);
+
+  // ---- producers: this thread's row and 32-column quarter of every step
+  const int trow = tid >> 2, quar = tid & 3;
+  const int64_t cb = a.cols / 16;  // scale bytes per row
+  const bool vec = (a.cols % 64) == 0 && (reinterpret_cast<uintptr_t>(a.codes) % 16) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.scales) % 4) == 0;
+  // step (tile t, column step ks) for this thread into ring slot `slot`: its
+  // two blocks' codes, and for an even quarter the scales of both quarters
+  auto fetch = [&](int64_t t, int64_t ks, int slot) {
+    uint8_t *sl = ring + (uint32_t)slot * kTcSlot;
+    uint8_t *dc = sl + tid * 16, *ds = sl + 8192 + (tid >> 1) * 4;
+    const int64_t row = t * kTcM + trow;
+    const int64_t col0 = ks * kTcK + 32 * quar;
+    if (vec && row < a.rows && col0 < a.cols) {  // whole blocks, 16-byte aligned codes, 4-byte aligned scales
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc_smem(dc)),
+                   "l"(a.codes + row * (a.cols / 2) + col0 / 2) : "memory");
+      if ((quar & 1) == 0)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc_smem(ds)), "l"(a.scales + row * cb + col0 / 16)
+                     : "memory");
+      return;
+    }
+    uint32_t w[4] = {0u, 0u, 0u, 0u}, sc = 0u;  // zero codes: zero weights
+    if (row < a.rows) {
+      const uint2 *crow = reinterpret_cast<const uint2 *>(a.codes) + row * cb;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int64_t col = col0 + 16 * j;
+        if (col < a.cols) {
+          const uint2 v = __ldg(crow + (col >> 4));
+          w[2 * j] = v.x;
+          w[2 * j + 1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t col = col0 + 16 * j;
+        if ((quar & 1) == 0 && col < a.cols) sc |= (uint32_t)__ldg(a.scales + row * cb + (col >> 4)) << (8 * j);
+      }
+    }
+    *reinterpret_cast<uint4 *>(dc) = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((quar & 1) == 0) *reinterpret_cast<uint32_t *>(ds) = sc;
+  };
+  int64_t ft = g0 / a.K, fks = g0 % a.K;  // the next step to fetch
+  auto fetch_next = [&](int slot) {
+    fetch(ft, fks, slot);
+    if (++fks == a.K) {
+      fks = 0;
+      ++ft;
+    }
+  };
+  if (warp < kTcProducers / 32) {
+#pragma unroll 1
+    for (int i = 0; i < D; ++i) {  // the ring's first D steps (one commit group each)
+      if (i < n) fetch_next(i);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+  }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = tmem_slot;
-  const uint32_t idesc = tc_idesc(N);
-  bool ok = true;  // uniform over the CTA
-  for (int s = 0; s < nsteps; ++s) {
-    const int st = s % S;
-    const int sn = (s + 1) % S;
-    if (s + 1 >= S) {  // stage sn was last read by the MMAs of step s + 1 - S
-      const int prev = s + 1 - S;
-      const bool arrived = tc_wait(tc_smem(&mbar[sn]), (uint32_t)((prev / S) & 1));
-      if (!__syncthreads_and(arrived)) {
-        ok = false;
-        break;
-      }
-    }
-    uint8_t *A = gbase + st * kStage + half * kAtomA;  // this thread's atom: columns 64*half ..
-    const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
-                            cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t w[8];
-      dequant16_bf16(make_uint2(cw[2 * j], cw[2 * j + 1]), s_tab[(cur.s >> (8 * j)) & 0xFFu], w);
-      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, 2u * j)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, 2u * j + 1u)) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this step's X has landed
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
-    __syncthreads();
-    // the next loads are issued after the proxy fence, which would otherwise wait for them
-    if (s + 1 < nsteps) issue_x(s + 1, sn);
-    load_codes(s + 2, nx2);
-    if (tid == 0) {
-      asm volatile("tcgen05.fence::after_thread_sync;");
-      const uint32_t a0 = base + st * kStage, b0 = a0 + kA;
-#pragma unroll
-      for (int kk = 0; kk < kTcK / 16; ++kk) {  // 4 K-slices of 16 in each of the two atoms
-        const uint32_t atom = (uint32_t)(kk >> 2), ko = 32u * (uint32_t)(kk & 3);
-        const uint64_t ad = tc_desc(a0 + atom * kAtomA + ko), bd = tc_desc(b0 + atom * kAtomB + ko);
-        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                     ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
-      }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                   ::"r"(tc_smem(&mbar[st])) : "memory");
-    }
-    cur = nx1;
-    nx1 = nx2;
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the CTA
-  if (ok) {  // the last commit covers every MMA of this CTA
-    const int last = nsteps - 1;
-    ok = __syncthreads_and(tc_wait(tc_smem(&mbar[last % S]), (uint32_t)((last / S) & 1)));
-  } else {   // give the MMAs already issued their time (bounded), then report NaN
-    for (int st = 0; st < S; ++st) tc_wait(tc_smem(&mbar[st]), 0u);
-  }
-  asm volatile("tcgen05.fence::after_thread_sync;");
-  float *dst = out + (int64_t)blockIdx.y * batch * rows;
-  const int64_t orow = row0 + tid;  // the row whose accumulator lane this thread reads (warps 0-3)
+
+  if (warp < kTcProducers / 32) {
+    // ---- dequantize: step i of this CTA goes to stage i % S and ring slot i % D
 #pragma unroll 1
-  for (int n0 = 0; n0 < N && warp < 4; n0 += 16) {  // warp w reads tensor-memory lanes 32w..32w+31
-    uint32_t r[16];
-    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)n0;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                 "%12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                   "=r"(r[15])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (orow < rows) {
+    for (int i = 0; i < n; ++i) {
+      const int st = i % S, slot = i % D;
+      // (the decision to leave is taken by the whole warp: __syncwarp below needs every lane)
+      const bool free_st = i < S || tc_wait(tc_smem(&empty[st]), (uint32_t)(((i - S) / S) & 1), vfail);
+      if (!__all_sync(0xFFFFFFFFu, free_st)) break;
+      asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");  // step i's codes have landed
+      const uint8_t *sl = ring + (uint32_t)slot * kTcSlot;
+      const uint4 c = *reinterpret_cast<const uint4 *>(sl + tid * 16);
+      uint32_t sc = (quar & 1) == 0 ? *reinterpret_cast<const uint32_t *>(sl + 8192 + (tid >> 1) * 4) : 0u;
+      sc = __shfl_sync(0xFFFFFFFFu, sc, lane & ~1) >> (16 * (quar & 1));  // this quarter's two scales
+      // columns 32*quar .. : atom quar / 2, 16-byte chunks 4 (quar % 2) ..
+      uint8_t *A = gbase + st * C::kStage + (quar >> 1) * C::kAtomA;
+      const uint32_t ch = 4u * (uint32_t)(quar & 1);
+      uint32_t w[8];
+      dequant16_bf16(make_uint2(c.x, c.y), s_tab[sc & 0xFFu], w);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, ch + 1u)) = make_uint4(w[4], w[5], w[6], w[7]);
+      dequant16_bf16(make_uint2(c.z, c.w), s_tab[(sc >> 8) & 0xFFu], w);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, ch + 2u)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4 *>(A + sw128((uint32_t)trow, ch + 3u)) = make_uint4(w[4], w[5], w[6], w[7]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tc_smem(&full[st]));
+      // the slot just read (its values are consumed above) takes step i + D
+      if (i + D < n) fetch_next(slot);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
+  } else if (warp == kTcMmaWarp) {
+    // ---- MMAs into accumulator (segment & 1)
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc(N);
+      // descriptors of stage 0's A and X atoms; stage s and K-slice kk add
+      // (s * kStage + atom offset + 32 kk) >> 4 to the start-address field
+      const uint64_t ad0 = tc_desc(base), bd0 = tc_desc(base + 2 * C::kAtomA);
+      int issued = 0;  // steps whose MMAs are committed: [0, issued)
+      int seg = -1;
+      int64_t ks = g0 % a.K;  // column step of step i
+#pragma unroll 1
+      for (int i = 0; i < n; ++i, ks = ks + 1 == a.K ? 0 : ks + 1) {
+        const int st = i % S;
+        const uint32_t ph = (uint32_t)((i / S) & 1);
+        const bool first = (i == 0) || ks == 0;
+        if (first) {
+          ++seg;
+          if (seg >= 2 && !tc_wait(tc_smem(&acc_empty[seg & 1]), (uint32_t)(((seg - 2) >> 1) & 1), vfail)) break;
+        }
+        if (!tc_wait(tc_smem(&full[st]), ph, vfail)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint64_t so = (uint64_t)((st * C::kStage) >> 4);
+        const uint32_t acc_t = tmem + (uint32_t)(seg & 1) * C::kCols;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (n0 + i < batch) dst[(int64_t)(n0 + i) * rows + orow] = ok ? __uint_as_float(r[i]) : __int_as_float(0x7FC00000);
+        for (int kk = 0; kk < kTcK / 16; ++kk) {  // 4 K-slices of 16 in each of the two atoms
+          const uint64_t ka = (uint64_t)(((kk >> 2) * C::kAtomA + 32u * (kk & 3)) >> 4);
+          const uint64_t kb = (uint64_t)(((kk >> 2) * C::kAtomB + 32u * (kk & 3)) >> 4);
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+          asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                       ::"r"(acc_t), "l"(ad0 + so + ka), "l"(bd0 + so + kb), "r"(idesc), "r"(acc));
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     ::"r"(tc_smem(&empty[st])) : "memory");
+        if (ks == a.K - 1 || i == n - 1)
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                       ::"r"(tc_smem(&acc_full[seg & 1])) : "memory");
+        issued = i + 1;
+      }
+      // after a failure: let the MMAs already issued finish before the CTA leaves
+      if (*vfail && issued > 0) tc_drain(tc_smem(&empty[(issued - 1) % S]), (uint32_t)(((issued - 1) / S) & 1));
+    }
+    __syncwarp();
+  } else if (warp == kTcXWarp) {
+    // ---- X by TMA: step i's N x 128 tile into stage i % S once the MMAs of step i - S are done
+    if (lane == 0) {
+      const uint64_t tmap = reinterpret_cast<uint64_t>(&xmap);
+      int64_t xks = g0 % a.K;
+      int x_hi = 0;  // steps whose X has been requested: [0, x_hi)
+#pragma unroll 1
+      for (int i = 0; i < n; ++i, xks = xks + 1 == a.K ? 0 : xks + 1) {
+        const int st = i % S;
+        if (i >= S && !tc_wait(tc_smem(&empty[st]), (uint32_t)(((i - S) / S) & 1), vfail)) break;
+        const uint32_t mb = tc_smem(&full[st]);
+        const uint32_t dst = base + st * C::kStage + 2 * C::kAtomA;
+        const int c0 = (int)(xks * kTcK);
+        mbar_expect_tx(mb, 2 * C::kAtomB);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                       " [%0], [%1, {%2, %3}], [%4];"
+                       ::"r"(dst + h * C::kAtomB), "l"(tmap), "r"(c0 + 64 * h), "r"(0), "r"(mb) : "memory");
+        x_hi = i + 1;
+      }
+      // after a failure: let the loads whose completion nothing has seen yet land
+      // (a load of step i was seen once the MMAs of step i were done; the
+      // phase of a later one may never complete when producers gave up, and
+      // then the bounded wait outlasts the copy)
+      if (*vfail)
+        for (int i = x_hi - S > 0 ? x_hi - S : 0; i < x_hi; ++i)
+          tc_drain(tc_smem(&full[i % S]), (uint32_t)((i / S) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ---- read back each segment's accumulator: warp w takes lanes 32 (w % 4) ..
+    const int q = warp & 3;
+    const int64_t c = blockIdx.x;
+#pragma unroll 1
+    for (int k = 0; k < nseg; ++k) {
+      if (!__all_sync(0xFFFFFFFFu, tc_wait(tc_smem(&acc_full[k & 1]), (uint32_t)((k >> 1) & 1), vfail))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const int64_t t = t_first + k;
+      const int64_t j = c - tc_cta_of(t * a.K, a.T, G);
+      float *dst = a.ws + ((t * a.maxc + j) * a.batch) * kTcM + q * 32 + lane;
+#pragma unroll 1
+      for (int n0 = 0; n0 < N && n0 < a.batch; n0 += 16) {
+        uint32_t r[16];
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(k & 1) * C::kCols + (uint32_t)n0;
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15}, [%16];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                       "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                       "=r"(r[14]), "=r"(r[15])
+                     : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (n0 + u < a.batch) dst[(int64_t)(n0 + u) * kTcM] = __uint_as_float(r[u]);
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tc_smem(&acc_empty[k & 1]));
     }
   }
+
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  if (*vfail && warp >= kTcEpiWarp0) {  // report the failure through every slot of this CTA
+    const int q = warp & 3;
+    for (int k = 0; k < nseg; ++k) {
+      const int64_t t = t_first + k;
+      const int64_t j = (int64_t)blockIdx.x - tc_cta_of(t * a.K, a.T, G);
+      float *dst = a.ws + ((t * a.maxc + j) * a.batch) * kTcM + q * 32 + lane;
+      for (int b = 0; b < a.batch; ++b) dst[(int64_t)b * kTcM] = __int_as_float(0x7FC00000);
+    }
+  }
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * C::kCols));
 }
 
-// y = sum over the splits of the partial products, in split order.
-__global__ void __launch_bounds__(256) k_gemm_tc_reduce(const float *__restrict__ part, int splits, int64_t n,
+// y[b][r] = the workspace slots of r's tile added in CTA order.
+__global__ void __launch_bounds__(256) k_gemm_tc_reduce(const float *__restrict__ ws, int64_t rows, int batch,
+                                                         int64_t K, int64_t T, int64_t G, int maxc,
                                                          float *__restrict__ y) {
+  const int64_t n = (int64_t)batch * rows;
   for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
-    float acc = part[i];
-    for (int sp = 1; sp < splits; ++sp) acc = __fadd_rn(acc, part[(int64_t)sp * n + i]);
+    const int64_t b = i / rows, r = i - b * rows, t = r / kTcM;
+    const int cnt = (int)(tc_cta_of((t + 1) * K - 1, T, G) - tc_cta_of(t * K, T, G)) + 1;
+    const float *p = ws + ((t * maxc) * batch + b) * kTcM + (r - t * kTcM);
+    const int64_t slot = (int64_t)batch * kTcM;
+    float acc = p[0];
+    for (int j = 1; j < cnt; ++j) acc = __fadd_rn(acc, p[j * slot]);
     y[i] = acc;
   }
 }
 
 namespace {
-template <int N>
-size_t tc_smem_bytes() { return TcStages<N>::value * 2 * ((size_t)kTcM * 128 + (size_t)N * 128) + 1024; }
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (the library does not link the driver library itself).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
 
 template <int N>
-cudaError_t tc_launch(dim3 grid, const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
-                      int64_t cols, const uint4 *x, int batch, int64_t kspan, float *out, cudaStream_t st) {
-  k_gemm_tc<N><<<grid, kTcThreads, tc_smem_bytes<N>(), st>>>(codes, scales, alpha, rows, cols, x, batch, kspan, out);
+cudaError_t tc_launch(const CUtensorMap &m, const TcArgs &a, int grid, cudaStream_t st) {
+  k_gemm_tc<N><<<grid, kTcThreads, TcCfg<N>::kSmem, st>>>(m, a);
   return cudaGetLastError();
 }
+
+struct TcPlan {
+  int64_t tiles, K, T, G;
+  int maxc;
+};
+
+TcPlan tc_plan(int64_t rows, int64_t cols, int sms) {
+  TcPlan p;
+  p.tiles = (rows + kTcM - 1) / kTcM;
+  p.K = (cols + kTcK - 1) / kTcK;
+  p.T = p.tiles * p.K;
+  p.G = std::min<int64_t>(p.T, sms);
+  // K consecutive steps meet at most (K - 1) / (shortest range) + 2 CTA ranges
+  const int64_t shortest = std::max<int64_t>(1, p.T / p.G);
+  p.maxc = (int)std::min<int64_t>(p.G, (p.K - 1) / shortest + 2);
+  return p;
+}
+
 }  // namespace
 
 int gemm_tc_tile_n(int batch) { return batch <= 16 ? 16 : batch <= 32 ? 32 : batch <= 64 ? 64 : batch <= 128 ? 128 : 256; }
 
-// Resident CTAs per SM of the tile width serving `batch`: the smallest of the
-// shared-memory, tensor-memory (512 columns), register and thread limits.
-int gemm_tc_ctas_per_sm(int batch) {
-  const int n = gemm_tc_tile_n(batch);
-  size_t smem = 0;
-  cudaFuncAttributes fa = {};
-  cudaError_t e;
-  switch (n) {
-    case 16: smem = tc_smem_bytes<16>(); e = cudaFuncGetAttributes(&fa, k_gemm_tc<16>); break;
-    case 32: smem = tc_smem_bytes<32>(); e = cudaFuncGetAttributes(&fa, k_gemm_tc<32>); break;
-    case 64: smem = tc_smem_bytes<64>(); e = cudaFuncGetAttributes(&fa, k_gemm_tc<64>); break;
-    case 128: smem = tc_smem_bytes<128>(); e = cudaFuncGetAttributes(&fa, k_gemm_tc<128>); break;
-    default: smem = tc_smem_bytes<256>(); e = cudaFuncGetAttributes(&fa, k_gemm_tc<256>); break;
-  }
-  int dev = 0, sm_smem = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-  if (e != cudaSuccess) return 1;
-  const size_t per_cta = smem + fa.sharedSizeBytes + 1024;  // + the per-CTA reservation
-  int c = (int)(sm_smem / per_cta);
-  c = std::min(c, 512 / (n <= 32 ? 32 : n));
-  if (fa.numRegs > 0) c = std::min(c, 65536 / (fa.numRegs * kTcThreads));
-  c = std::min(c, 2048 / kTcThreads);
-  return c < 1 ? 1 : c;
+size_t gemm_tc_workspace_bytes(int64_t rows, int64_t cols, int batch, int sms) {
+  const TcPlan p = tc_plan(rows, cols, sms);
+  return sizeof(float) * (size_t)(p.tiles * p.maxc) * (size_t)batch * kTcM;
 }
 
 cudaError_t launch_gemm_tc(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
-                           int64_t cols, const void *x, int batch, int64_t kspan, int splits, float *out,
-                           cudaStream_t st) {
-  const dim3 grid((unsigned)((rows + kTcM - 1) / kTcM), (unsigned)splits);
-  const uint4 *xv = static_cast<const uint4 *>(x);
-  switch (gemm_tc_tile_n(batch)) {
-    case 16: return tc_launch<16>(grid, codes, scales, alpha, rows, cols, xv, batch, kspan, out, st);
-    case 32: return tc_launch<32>(grid, codes, scales, alpha, rows, cols, xv, batch, kspan, out, st);
-    case 64: return tc_launch<64>(grid, codes, scales, alpha, rows, cols, xv, batch, kspan, out, st);
-    case 128: return tc_launch<128>(grid, codes, scales, alpha, rows, cols, xv, batch, kspan, out, st);
-    default: return tc_launch<256>(grid, codes, scales, alpha, rows, cols, xv, batch, kspan, out, st);
+                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, cudaStream_t st) {
+  if (!g_encode) return cudaErrorInitializationError;
+  const TcPlan p = tc_plan(rows, cols, sms);
+  const int n = gemm_tc_tile_n(batch);
+  // X [batch, cols] bf16, boxes of 64 columns x n rows (rows past the batch
+  // and columns past the end read as zeros), 128-byte swizzle
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)batch};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)n};
+  const cuuint32_t es[2] = {1u, 1u};
+  if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const TcArgs a = {codes, scales, alpha, rows, cols, batch, p.K, p.T, p.maxc, ws};
+  const int grid = (int)p.G;
+  cudaError_t e;
+  switch (n) {
+    case 16: e = tc_launch<16>(m, a, grid, st); break;
+    case 32: e = tc_launch<32>(m, a, grid, st); break;
+    case 64: e = tc_launch<64>(m, a, grid, st); break;
+    case 128: e = tc_launch<128>(m, a, grid, st); break;
+    default: e = tc_launch<256>(m, a, grid, st); break;
   }
+  return e;
 }
 
-cudaError_t launch_gemm_tc_reduce(const float *part, int splits, int64_t n, float *y, int grid, cudaStream_t st) {
-  k_gemm_tc_reduce<<<grid, 256, 0, st>>>(part, splits, n, y);
+cudaError_t launch_gemm_tc_reduce(const float *ws, int64_t rows, int64_t cols, int batch, int sms, float *y,
+                                  int grid, cudaStream_t st) {
+  const TcPlan p = tc_plan(rows, cols, sms);
+  k_gemm_tc_reduce<<<grid, 256, 0, st>>>(ws, rows, batch, p.K, p.T, p.G, p.maxc, y);
   return cudaGetLastError();
 }
 
 cudaError_t prepare_gemm_tc_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<16>());
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<32>());
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<64>());
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<128>());
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes<256>());
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<16>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<32>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<64>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<128>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<256>::kSmem);
   return e;
 }
 

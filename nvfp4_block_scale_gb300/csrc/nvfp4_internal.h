@@ -56,11 +56,11 @@ cudaError_t prepare_gemv_kernels();
 cudaError_t launch_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t kb, uint8_t *out,
                                   cudaStream_t st);
 int gemm_tc_tile_n(int batch);
-int gemm_tc_ctas_per_sm(int batch);
+size_t gemm_tc_workspace_bytes(int64_t rows, int64_t cols, int batch, int sms);
 cudaError_t launch_gemm_tc(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
-                           int64_t cols, const void *x, int batch, int64_t kspan, int splits, float *out,
-                           cudaStream_t st);
-cudaError_t launch_gemm_tc_reduce(const float *part, int splits, int64_t n, float *y, int grid, cudaStream_t st);
+                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, cudaStream_t st);
+cudaError_t launch_gemm_tc_reduce(const float *ws, int64_t rows, int64_t cols, int batch, int sms, float *y,
+                                  int grid, cudaStream_t st);
 cudaError_t prepare_gemm_tc_kernels();
 cudaError_t prepare_decoupled_kernel();
 int max_active_ctas(int which);

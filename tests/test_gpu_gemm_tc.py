@@ -3,9 +3,12 @@ tensor memory), against the oracle's product of the dequantized bf16 weights
 summed in double.  Every product is exact; the tensor cores accumulate in
 fp32 in an order of their own, so the bar is 2 * (cols + 2) * 2^-24 *
 sum |w x| per output (twice the bound of any order of fp32 additions plus
-the split-K additions).  Ragged rows and K steps, every tile width (16..256
-vectors), split and unsplit K, all four scale rules, and the benchmark's
-8192x28672 tensor on sampled rows."""
+the additions of the partial sums of CTAs that share a tile).  Ragged rows
+and K steps, every tile width (16..256 vectors), CTAs whose step ranges
+cover one step, part of a tile or several whole tiles (so the double-buffered
+accumulator is reused), code and scale arrays that are not 16-byte aligned,
+all four scale rules, and the benchmark's 8192x28672 tensor on sampled
+rows."""
 import numpy as np
 import pytest
 import torch
@@ -70,3 +73,35 @@ def test_gemm_full_size_sampled_rows():
     c, s, a = codes.cpu().numpy(), scales.cpu().numpy(), alpha.item()
     for r0 in (0, rows // 2 + 5, rows - 24):
         _check(c[r0:r0 + 24], s[r0:r0 + 24], a, 24, cols, x_bits, y[:, r0:r0 + 24])
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(51200, 128, 16), (40000, 64, 200), (30000, 192, 33), (1, 4096, 5)])
+def test_gemm_ctas_spanning_several_tiles(rows, cols, batch):
+    # 128-column steps: K = 1 or 2 per tile, so one CTA's range covers 2-3 tiles
+    # (three or more accumulators in a row); the last case gives every CTA one step
+    w = synthetic.gaussian(rows, cols, 0.02, 9300 + rows)
+    codes, scales, alpha = nv.quantize(to_device(w), nv.MAX)
+    x_bits = _acts(batch, cols, 9301 + batch)
+    y = nv.gemm(codes, scales, alpha, rows, cols, to_device(x_bits))
+    torch.cuda.synchronize()
+    _check(codes.cpu().numpy(), scales.cpu().numpy(), alpha.item(), rows, cols, x_bits, y.cpu().numpy())
+
+
+def test_gemm_unaligned_codes_and_scales():
+    # codes 8 bytes and scales 1 byte past a 16-byte boundary: the per-block load path
+    rows, cols, batch = 384, 2048, 12
+    w = synthetic.student_t(rows, cols, 4.0, 0.02, 9400)
+    codes, scales, alpha = nv.quantize(to_device(w), nv.FOUR_OVER_SIX)
+    cbuf = torch.zeros(codes.numel() + 16, dtype=torch.uint8, device="cuda")
+    sbuf = torch.zeros(scales.numel() + 16, dtype=torch.uint8, device="cuda")
+    c8 = cbuf[8:8 + codes.numel()]
+    s1 = sbuf[1:1 + scales.numel()]
+    c8.copy_(codes.reshape(-1))
+    s1.copy_(scales.reshape(-1))
+    x_bits = _acts(batch, cols, 9401)
+    x = to_device(x_bits)
+    y = nv.gemm(c8, s1, alpha, rows, cols, x)
+    ref = nv.gemm(codes, scales, alpha, rows, cols, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)  # same steps, same order: only the load path differs
+    _check(codes.cpu().numpy(), scales.cpu().numpy(), alpha.item(), rows, cols, x_bits, y.cpu().numpy())
