@@ -15,21 +15,25 @@
 // sum goes to a workspace slot and k_gemm_tc_reduce adds the slots of a tile
 // in CTA order (a fixed order: the result does not depend on timing).
 //
-// Roles inside a CTA (704 threads):
-//   - warps 0-15 (512 threads, four per row of the tile) dequantize.  Each
-//     thread keeps its own 16 code bytes per step (and every other thread
-//     the 4 scale bytes of itself and its neighbour) for the next D steps in
-//     flight in a shared-memory ring (cp.async), and per step writes its 32
-//     bf16 weights into the 128 x 128 A tile of the stage (K-major, 128-byte
+// Roles inside a CTA (768 threads), every hand-off through an mbarrier:
+//   - warps 0-15 (512 threads, four per row of the tile) dequantize: per step
+//     each reads its 16 code bytes and two scales from a ring slot and writes
+//     its 32 bf16 weights into the stage's 128 x 128 A tile (K-major, 128-byte
 //     swizzle);
-//   - warp 16 (one lane) issues per step eight tcgen05.mma (kind::f16,
-//     bf16 x bf16 -> fp32, M = 128, K = 16 each) into a tensor-memory
-//     accumulator and commits them to the stage's mbarrier;
-//   - warp 17 (one lane) loads the N x 128 tile of X per step with TMA (the
-//     tensor map's 128-byte swizzle gives the layout the MMA reads) as soon as
-//     the stage's previous MMAs are done;
-//   - warps 18-21 read each finished accumulator back with tcgen05.ld (the
-//     accumulator is double-buffered, so this overlaps the next segment).
+//   - warp 19 (one lane) fills the ring by TMA, one slot per step: the tile's
+//     128 x 64 code bytes and the 128 x 16 scale bytes holding the step's 8.
+//     Where rows of codes or scales are not whole multiples of 16 bytes, the
+//     producer threads instead keep their own bytes in flight with cp.async;
+//   - warp 18 (one lane) loads the N x 128 tile of X per step with TMA (the
+//     tensor map's 128-byte swizzle gives the layout the MMA reads) once the
+//     stage's previous MMAs are done;
+//   - warps 16 and 17 (one lane each) issue the eight tcgen05.mma (kind::f16,
+//     bf16 x bf16 -> fp32, M = 128, K = 16 each) of every other step into
+//     their own accumulator of a pair in tensor memory, and commit them to the
+//     stage's mbarrier;
+//   - warps 20-23 read each finished pair back with tcgen05.ld and add it in
+//     a fixed order (pairs are double-buffered for N <= 128, so this overlaps
+//     the next segment).
 // Every mbarrier wait is bounded; a CTA that gives up waits (bounded) for its
 // own copies and MMAs in flight, writes NaN to its workspace slots and frees
 // its tensor memory.
@@ -529,27 +533,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmem));
 }
 
-// y[b][r] = the workspace slots of r's tile added in CTA order (the loads of
-// up to four slots are issued together; the additions keep that order).
+// y[b][r] = the workspace slots of r's tile added in CTA order.  A thread
+// takes 4 consecutive rows of one tile and batch column (16-byte loads of
+// every slot issued together; the additions keep the slot order).
 __global__ void __launch_bounds__(256) k_gemm_tc_reduce(const float *__restrict__ ws, int64_t rows, int batch,
                                                          int64_t K, int64_t T, int64_t G, int maxc,
                                                          float *__restrict__ y) {
-  const int64_t n = (int64_t)batch * rows;
+  const int64_t tiles = (rows + kTcM - 1) / kTcM;
+  const int64_t n = (int64_t)batch * tiles * (kTcM / 4);  // groups of 4 rows
   const int64_t slot = (int64_t)batch * kTcM;
-  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
-    const int64_t b = i / rows, r = i - b * rows, t = r / kTcM;
+  const bool vec_y = (rows % 4) == 0 && (reinterpret_cast<uintptr_t>(y) % 16) == 0;
+  for (int64_t g = (int64_t)blockIdx.x * 256 + threadIdx.x; g < n; g += (int64_t)gridDim.x * 256) {
+    const int64_t rg = g % (tiles * (kTcM / 4)), b = g / (tiles * (kTcM / 4));
+    const int64_t t = rg / (kTcM / 4), r0 = t * kTcM + (rg % (kTcM / 4)) * 4;
+    if (r0 >= rows) continue;
     const int cnt = (int)(tc_cta_of((t + 1) * K - 1, T, G) - tc_cta_of(t * K, T, G)) + 1;
-    const float *p = ws + ((t * maxc) * batch + b) * kTcM + (r - t * kTcM);
-    const float v0 = p[0];
-    const float v1 = cnt > 1 ? p[slot] : 0.0f;
-    const float v2 = cnt > 2 ? p[2 * slot] : 0.0f;
-    const float v3 = cnt > 3 ? p[3 * slot] : 0.0f;
-    float acc = v0;
-    if (cnt > 1) acc = __fadd_rn(acc, v1);
-    if (cnt > 2) acc = __fadd_rn(acc, v2);
-    if (cnt > 3) acc = __fadd_rn(acc, v3);
-    for (int j = 4; j < cnt; ++j) acc = __fadd_rn(acc, p[j * slot]);
-    y[i] = acc;
+    const float4 *p = reinterpret_cast<const float4 *>(ws + ((t * maxc) * batch + b) * kTcM + (r0 - t * kTcM));
+    const int64_t s4 = slot / 4;
+    const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float4 v0 = p[0], v1 = cnt > 1 ? p[s4] : z, v2 = cnt > 2 ? p[2 * s4] : z, v3 = cnt > 3 ? p[3 * s4] : z;
+    float4 acc = v0;
+    auto add = [](float4 &x, const float4 &u) {
+      x.x = __fadd_rn(x.x, u.x);
+      x.y = __fadd_rn(x.y, u.y);
+      x.z = __fadd_rn(x.z, u.z);
+      x.w = __fadd_rn(x.w, u.w);
+    };
+    if (cnt > 1) add(acc, v1);
+    if (cnt > 2) add(acc, v2);
+    if (cnt > 3) add(acc, v3);
+    for (int j = 4; j < cnt; ++j) add(acc, p[j * s4]);
+    float *o = y + b * rows + r0;
+    if (vec_y && r0 + 4 <= rows) {
+      *reinterpret_cast<float4 *>(o) = acc;
+    } else {
+      const float w[4] = {acc.x, acc.y, acc.z, acc.w};
+      for (int u = 0; u < 4 && r0 + u < rows; ++u) o[u] = w[u];
+    }
   }
 }
 
