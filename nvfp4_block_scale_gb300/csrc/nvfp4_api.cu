@@ -39,6 +39,11 @@ struct DevInfo {
   int l2 = 0;  // L2 bytes
   int occ[kKernCount] = {};
   cudaMemPool_t pool = nullptr;
+  // second stream and fork/join events of the pipelined grouped quantization;
+  // `side_mu` keeps one caller at a time on them
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex side_mu;
 };
 
 std::mutex g_mu;
@@ -84,6 +89,9 @@ int device_info(DevInfo **out) {
       if (e != cudaSuccess) return map_cuda(e);
       uint64_t keep = UINT64_MAX;
       e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
       if (e != cudaSuccess) return map_cuda(e);
       d.status = NVFP4_OK;
     }
@@ -297,18 +305,45 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
     return NVFP4_OK;
   }
 
-  const int nslices = (count + kGroupMax - 1) / kGroupMax;
+  // Parts of at most kGroupMax tensors, each an amax pass and a quantize pass
+  // over its tiles.  A large group (at least 16 x L2 of bf16) is cut into 8
+  // parts of about equal size that alternate between the caller's stream and
+  // the library's second stream, so one part's amax pass (HBM-bound) runs
+  // beside another's quantize pass (ALU-bound); small groups keep one part
+  // per kGroupMax tensors, which lets the quantize pass re-read from L2 what
+  // the amax pass read last.
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) total += tensors[i].rows * tensors[i].cols;
+  const bool pipe = total * 2 >= int64_t(16) * d->l2 && count >= 2;
+  std::vector<int> cut;  // part k covers tensors [cut[k], cut[k + 1])
+  cut.push_back(0);
+  const int parts = pipe ? 8 : 1;
+  int64_t acc = 0;
+  for (int i = 0; i + 1 < count; ++i) {  // a cut after tensor i where 1/parts of the elements is passed
+    acc += tensors[i].rows * tensors[i].cols;
+    if ((pipe && acc * parts >= total * (int64_t)cut.size()) || i + 1 - cut.back() == kGroupMax) cut.push_back(i + 1);
+  }
+  cut.push_back(count);
+  const int nparts = (int)cut.size() - 1;
   const size_t slot = (size_t)round_up(int64_t(kGroupMax) * 4, 256);
   void *ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, slot * nslices, d->pool, stream);
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, slot * nparts, d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
-  e = cudaMemsetAsync(ws, 0, slot * nslices, stream);  // every tensor's max|W| word starts at 0
+  e = cudaMemsetAsync(ws, 0, slot * nparts, stream);  // every tensor's max|W| word starts at 0
+  std::unique_lock<std::mutex> side_lock(d->side_mu, std::defer_lock);
+  if (pipe && e == cudaSuccess) {  // fork the second stream off the caller's
+    side_lock.lock();
+    e = cudaEventRecord(d->fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->side, d->fork, 0);
+  }
   GroupArgs *g = new (std::nothrow) GroupArgs;
   if (!g && e == cudaSuccess) e = cudaErrorMemoryAllocation;
   const int kq = mode == kModeFourOverSix ? kKernGroupQuantFos : kKernGroupQuantMax;
   const int64_t full = int64_t(d->sms) * std::min(d->occ[kKernGroupAmax], d->occ[kq]);
-  for (int s0 = 0; s0 < count && e == cudaSuccess; s0 += kGroupMax) {
-    g->count = std::min(kGroupMax, count - s0);
+  for (int k = 0; k < nparts && e == cudaSuccess; ++k) {
+    const int s0 = cut[k];
+    cudaStream_t ps = pipe && (k & 1) ? d->side : stream;
+    g->count = cut[k + 1] - s0;
     g->tile_begin[0] = 0;
     for (int i = 0; i < g->count; ++i) {
       const nvfp4_tensor &x = tensors[s0 + i];
@@ -322,17 +357,22 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
     }
     const int64_t tiles = g->tile_begin[g->count];
     const int grid = (int)std::max<int64_t>(1, std::min(full, tiles));
-    uint32_t *amax = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + slot * (s0 / kGroupMax));
+    uint32_t *amax = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + slot * k);
     {
-      TraceScope tr(kTrGroupAmax, stream);
-      e = launch_group_amax(*g, amax, grid, stream);
+      TraceScope tr(kTrGroupAmax, ps);
+      e = launch_group_amax(*g, amax, grid, ps);
     }
     if (e == cudaSuccess) {
-      TraceScope tr(mode == kModeFourOverSix ? kTrGroupQuantFos : kTrGroupQuantMax, stream);
-      e = launch_group_quant(mode, *g, amax, grid, stream);
+      TraceScope tr(mode == kModeFourOverSix ? kTrGroupQuantFos : kTrGroupQuantMax, ps);
+      e = launch_group_quant(mode, *g, amax, grid, ps);
     }
   }
   delete g;
+  if (side_lock.owns_lock()) {  // join: the caller's stream waits for the second stream's parts
+    cudaError_t ej = cudaEventRecord(d->join, d->side);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, d->join, 0);
+    if (e == cudaSuccess) e = ej;
+  }
   cudaError_t ef = cudaFreeAsync(ws, stream);
   return map_cuda(e != cudaSuccess ? e : ef);
 }

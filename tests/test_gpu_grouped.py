@@ -1,8 +1,9 @@
 """nvfp4_quantize_grouped: every tensor of a group comes out exactly as the
 single-tensor call (and the oracle) gives it, whatever its size, position in
 the group or neighbours: tiny and ragged tensors, all-zero and empty ones,
-tensors of several tiles, and groups longer than one slice of
-NVFP4_GROUP_MAX tensors."""
+tensors of several tiles, groups longer than one slice of NVFP4_GROUP_MAX
+tensors, and groups large enough to be cut into parts that alternate between
+two streams (also under CUDA-graph capture)."""
 import numpy as np
 import pytest
 import torch
@@ -114,3 +115,41 @@ def test_grouped_full_llama3_stack_matches_single_calls():
         rc, rs, ra = nv.quantize(W, nv.FOUR_OVER_SIX)
         assert torch.equal(c, rc) and torch.equal(s, rs) and a.item() == ra.item()
         del rc, rs, ra
+
+
+def _large_group():
+    """112 tensors, 2.2 GiB of bf16 (beyond 16 x L2): the grouped call cuts it into
+    parts that alternate between two streams."""
+    g = torch.Generator(device="cuda").manual_seed(77)
+    shapes = [(4096, 4096), (1024, 4096), (3000, 2064), (14336, 1024)] * 28
+    return [(torch.randn(r, c, generator=g, device="cuda") * (0.01 + 0.001 * (i % 7))).to(torch.bfloat16)
+            for i, (r, c) in enumerate(shapes)]
+
+
+@pytest.mark.parametrize("mode", [nv.MAX, nv.FOUR_OVER_SIX])
+def test_grouped_two_stream_parts_match_single_calls(mode):
+    Ws = _large_group()
+    assert sum(W.numel() for W in Ws) * 2 >= 16 * torch.cuda.get_device_properties(0).L2_cache_size
+    outs = nv.quantize_grouped(Ws, mode)
+    torch.cuda.synchronize()
+    for W, (c, s, a) in zip(Ws, outs):
+        rc, rs, ra = nv.quantize(W, mode)
+        assert torch.equal(c, rc) and torch.equal(s, rs) and a.item() == ra.item()
+
+
+def test_grouped_two_stream_parts_under_graph_capture():
+    Ws = _large_group()
+    outs = nv.quantize_grouped(Ws, nv.FOUR_OVER_SIX)  # first call outside any capture
+    torch.cuda.synchronize()
+    ref = [(c.clone(), s.clone(), a.clone()) for c, s, a in outs]
+    for c, s, a in outs:
+        c.fill_(0xA5)
+        s.fill_(0xA5)
+        a.fill_(-1.0)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):  # the fork to the library's second stream joins back inside the capture
+        nv.quantize_grouped(Ws, nv.FOUR_OVER_SIX, outs=outs)
+    gr.replay()
+    torch.cuda.synchronize()
+    for (c, s, a), (rc, rs, ra) in zip(outs, ref):
+        assert torch.equal(c, rc) and torch.equal(s, rs) and torch.equal(a, ra)
