@@ -113,7 +113,13 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
  *           the rules of nvfp4_quantize.  Outputs of different tensors must
  *           not overlap each other or any W.
  *   count   >= 0 (0: nothing is enqueued).  Longer lists are processed in
- *           consecutive slices of NVFP4_GROUP_MAX tensors.
+ *           consecutive slices of NVFP4_GROUP_MAX tensors.  A list holding at
+ *           least 16 x L2 bytes of bf16 is cut into 8 parts of about equal
+ *           size that alternate between `stream` and a second stream owned
+ *           by the library (forked from `stream` and joined back into it by
+ *           events, so the call can be captured in a CUDA graph), letting one
+ *           part's max|W| pass overlap another part's quantize pass; calls
+ *           from several host threads take turns on that second stream.
  *   mode, iters, stream  as for nvfp4_quantize.  Modes 2 and 3 run the
  *           nvfp4_quantize launch sequence tensor by tensor (their search and
  *           sweeps, not launches, dominate).
