@@ -122,7 +122,8 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
  *           from several host threads take turns on that second stream.
  *   mode, iters, stream  as for nvfp4_quantize.  Modes 2 and 3 run the
  *           nvfp4_quantize launch sequence tensor by tensor (their search and
- *           sweeps, not launches, dominate).
+ *           sweeps, not launches, dominate), tensors alternating between
+ *           `stream` and the second stream.
  * Every descriptor is checked before anything is enqueued; the first bad one
  * decides the returned status.
  */

@@ -297,12 +297,27 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
   if (st != NVFP4_OK) return st;
   if (count == 0) return NVFP4_OK;
   if (cjso) {
-    for (int i = 0; i < count; ++i) {
-      const nvfp4_tensor &x = tensors[i];
-      st = nvfp4_quantize(x.W, x.rows, x.cols, mode, iters, x.codes, x.scales, x.alpha, stream);
-      if (st != NVFP4_OK) return st;
+    // the single-tensor sequence per tensor, tensors alternating between the
+    // caller's stream and the library's second one, so that one tensor's
+    // sweeps (HBM-bound) can run beside another's search (ALU-bound)
+    std::unique_lock<std::mutex> side_lock(d->side_mu, std::defer_lock);
+    cudaError_t e = cudaSuccess;
+    if (count >= 2) {
+      side_lock.lock();
+      e = cudaEventRecord(d->fork, stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->side, d->fork, 0);
     }
-    return NVFP4_OK;
+    for (int i = 0; i < count && e == cudaSuccess && st == NVFP4_OK; ++i) {
+      const nvfp4_tensor &x = tensors[i];
+      st = nvfp4_quantize(x.W, x.rows, x.cols, mode, iters, x.codes, x.scales, x.alpha,
+                          side_lock.owns_lock() && (i & 1) ? d->side : stream);
+    }
+    if (side_lock.owns_lock()) {  // join, also after an error
+      cudaError_t ej = cudaEventRecord(d->join, d->side);
+      if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, d->join, 0);
+      if (e == cudaSuccess) e = ej;
+    }
+    return st != NVFP4_OK ? st : map_cuda(e);
   }
 
   // Parts of at most kGroupMax tensors, each an amax pass and a quantize pass

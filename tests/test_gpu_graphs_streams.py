@@ -26,6 +26,10 @@ def _pipeline(W, X, outs):
     res.append(outs["swz"].copy_(nv.swizzle_scales(s, rows, cols)))
     for (gc, gs, ga) in nv.quantize_grouped([W, W[: rows // 2]], nv.MAX, outs=outs["grp"]):
         res += [gc, gs, ga]
+    # CJSO groups alternate tensors between the caller's stream and the library's second one
+    for (gc, gs, ga) in nv.quantize_grouped([W, W[: rows // 2], W[rows // 2:]], nv.CJSO_DECOUPLED, 1,
+                                            outs=outs["grp3"]):
+        res += [gc, gs, ga]
     return res
 
 
@@ -40,6 +44,7 @@ def _outs(rows, cols, batch):
     o["gemm"] = torch.empty((batch, rows), dtype=torch.float32, device=d)
     o["swz"] = torch.empty(nv.nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=d)
     o["grp"] = [q(rows), q(rows // 2)]
+    o["grp3"] = [q(rows), q(rows // 2), q(rows - rows // 2)]
     return o
 
 
