@@ -1,22 +1,34 @@
-"""Benchmark: NVFP4 quantize throughput (GB/s of bf16 input) on one GB300.
+"""Benchmark: NVFP4 quantize throughput (GB/s of bf16) on one GB300.
 
-Headline workload: the 4096x4096 bf16 Student-t (df=4, std 0.02) tensor with
-0.1 % outlier columns x20; one step = quantize it with the max rule and with
-FourOverSix (the two scale rules this workload is quoted on).  Enough device
-copies of the input rotate (> 2x L2) that every step starts from HBM.
+Headline workload: the 8192x28672 bf16 tensor (70B-style MLP, N(0, 0.01) with
+0.05 % of the entries set to +-U(0.3, 1)).  One step = the whole hot path on
+it: quantize with the max rule, FourOverSix, CJSO(5) and decoupled CJSO(5),
+then dequantize, back to back (20 steps by default: the sustained form).  The
+tensor (448 MiB) is larger than L2, and two device copies alternate, so every
+step reads W from HBM.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-                    [--workload NAME --modes a,b --iters T] [--quick]
+                    [--workload NAME --modes a,b --iters T] [--no-stack] [--quick]
 
-Prints one JSON line (rank 0).  `value` = bf16 input bytes of all ranks'
-steps / device time of the K steps (CUDA-graph replays of the C-ABI call
-sequence; CUDA events on the launching stream; barrier + synchronize on both
-sides; max over ranks).  `per_mode` = each mode alone, with per-kernel device
-times from the library's own per-launch CUDA events.  `roofline` = the
-heaviest mode of the step against its bound (HBM copy bandwidth, or the fp32
-pipe for the decoupled search).  `e2e` = the same metric through the C ABI with
-pinned host buffers (H2D of W, D2H of codes/scales/alpha inside the timed
-region).  `cpu_baseline` = the C oracle on the host cores (rank 0, N=1).
+Prints one JSON line (rank 0).
+  value        bf16 bytes of all ranks' steps (2 bytes per element for every
+               mode: the quantizers' input, the dequantizer's output) / device
+               time of the K steps (CUDA-graph replays of the C-ABI call
+               sequence; CUDA events on the launching stream; barrier +
+               synchronize on both sides; max over ranks).
+  per_mode     each mode alone: call time, GB/s, its roofline (HBM copy
+               bandwidth, or the measured fp32 FMA peak for the decoupled
+               search), per-kernel device times (the library's per-launch CUDA
+               events), reconstruction MSE in double, the M=4 block share of
+               FourOverSix, and the C oracle on the host cores on a bounded
+               sample of the same tensor.
+  roofline     the dominant kernel of the step (largest share of the step's
+               device time) against its bound.
+  e2e          the same step through the C ABI with pinned host buffers: H2D of
+               W and D2H of every output inside the timed region.
+  workloads    the 224-tensor Llama-3-8B-shaped stack (FourOverSix grouped,
+               decoupled CJSO(5)) as a second record (skipped with --no-stack
+               or N > 1).
 
 --impl reference runs the C oracle on a bounded sample of the same workload
 per step and prints the same line with "impl": "reference".
@@ -40,10 +52,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
-HEADLINE = "studentt_4k"
+HEADLINE = "mlp_70b"
 MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5, "swizzle": 6,
             "gemm": 7}
 CONSUMERS = ("dequant", "gemv", "swizzle", "gemm")  # modes that read a quantized tensor instead of producing one
+HOT_PATH = ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")
 
 
 def _synth():
@@ -53,18 +66,15 @@ def _synth():
 
 # name -> (generator(rank), description, default modes)
 WORKLOADS = {
+    "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
+                "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)", HOT_PATH),
     "studentt_4k": (lambda r: _synth().studentt_4k(seed=1 + r),
                     "4096x4096 bf16, Student-t df=4 std 0.02, 0.1% columns x20 (seed 1 + rank)",
                     ("max", "four_over_six")),
     "gauss_1k": (lambda r: _synth().gauss_1k(seed=0 + r),
-                 "1024x1024 bf16, N(0,0.02) (seed 0 + rank)",
-                 ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")),
+                 "1024x1024 bf16, N(0,0.02) (seed 0 + rank)", HOT_PATH),
     "mlp_up": (lambda r: _synth().mlp_up(seed=2 + r),
-               "4096x14336 bf16, 10% rows N(0,0.05), rest N(0,0.015) (seed 2 + rank)",
-               ("max", "four_over_six", "cjso", "cjso_decoupled")),
-    "mlp_70b": (lambda r: _synth().mlp_70b(seed=4 + r),
-                "8192x28672 bf16, N(0,0.01), 0.05% entries +-U(0.3,1) (seed 4 + rank)",
-                ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant", "gemv", "swizzle")),
+               "4096x14336 bf16, 10% rows N(0,0.05), rest N(0,0.015) (seed 2 + rank)", HOT_PATH),
 }
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy bandwidth is the roofline)
@@ -74,6 +84,8 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 
 
 def kernels_per_call(mode: int, iters: int) -> int:
+    """Kernels one call launches: amax + quantize; amax + init sweep + one
+    sweep per iteration (+ the search); one kernel for the consumers."""
     return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1, 7: 2}[mode]
 
 
@@ -186,8 +198,8 @@ def measured_bf16_tflops():
         return 1900.0, "fallback"
 
 
-def fp32_peak_tflops(sms: int, mhz: float) -> float:
-    """FP32 FMA peak: SMs x 128 lanes x 2 flop x clock."""
+def fp32_peak_derived(sms: int, mhz: float) -> float:
+    """FP32 FMA peak from the unit count: SMs x 128 lanes x 2 flop x clock."""
     return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
@@ -200,13 +212,13 @@ def source_digest() -> str:
 
 
 def recorded_traffic(key: str):
-    """DRAM bytes per call from the committed ncu summary, if taken on the
-    current kernel sources; else None."""
+    """DRAM bytes per launch (or call) from the committed ncu summary, if taken
+    on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         e = json.load(open(p))[key]
         if e.get("source_digest") == source_digest():
-            return e["dram_bytes_per_call"]
+            return e["dram_bytes"]
     except Exception:
         pass
     return None
@@ -233,24 +245,77 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=10.0, max_rows=None):
-    """The oracle as it stands on all host cores; the first `max_rows` rows."""
+def input_sha256(w_bits: np.ndarray) -> str:
+    return hashlib.sha256(np.ascontiguousarray(w_bits).tobytes()).hexdigest()
+
+
+def oracle_rows(mode: str, cols: int, rows: int) -> int:
+    """Rows of the bounded CPU sample per mode (a few seconds of oracle work on
+    16 host cores): the decoupled search is ~100x slower per element."""
+    budget = {"max": 1 << 23, "four_over_six": 1 << 23, "cjso": 1 << 22, "cjso_decoupled": 1 << 18,
+              "dequant": 1 << 23}[mode]
+    return int(max(16, min(rows, budget // cols)))
+
+
+def oracle_time_mode(w_bits, mode: str, iters: int, min_seconds: float):
+    """The oracle as it stands, on all host cores, on the first rows of W;
+    returns (GB/s of bf16, seconds, repetitions, rows)."""
     import oracle
     threads = os.cpu_count() or 1
-    sample = w_bits if max_rows is None else w_bits[:max_rows]
+    rows = oracle_rows(mode, w_bits.shape[1], w_bits.shape[0])
+    sample = np.ascontiguousarray(w_bits[:rows])
+    if mode == "dequant":
+        c, s, a = oracle.quantize(sample, oracle.MAX, 0, threads=threads)
+        fn = lambda: oracle.dequantize(c, s, a, rows, sample.shape[1])
+    else:
+        fn = lambda: oracle.quantize(sample, MODE_IDS[mode], iters, threads=threads)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        for m in modes:
-            oracle.quantize(sample, MODE_IDS[m], iters, threads=threads)
+        fn()
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
             break
-    gbs = reps * len(modes) * sample.nbytes / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"rows 0..{sample.shape[0] - 1} of {w_bits.shape[0]}x{w_bits.shape[1]}, "
-                      f"{'+'.join(modes)}, {reps} repetition(s) in {el:.1f} s"}
+    return reps * sample.nbytes / el / 1e9, el, reps, rows
+
+
+def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=4.0):
+    """Per mode and for the whole step: the oracle on host cores, bounded samples."""
+    threads = os.cpu_count() or 1
+    per, tot_bytes, tot_s = {}, 0.0, 0.0
+    for m in modes:
+        gbs, el, reps, rows = oracle_time_mode(w_bits, m, iters, min_seconds)
+        per[m] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                  "sample": f"rows 0..{rows - 1} of {w_bits.shape[0]}x{w_bits.shape[1]}, {reps} repetition(s) "
+                            f"in {el:.1f} s" + (" (dequantize of the max-rule output)" if m == "dequant" else "")}
+        tot_bytes += w_bits.shape[1] * 2  # one row of bf16 per mode: combine per-row costs
+        tot_s += w_bits.shape[1] * 2 / (gbs * 1e9)
+    step = {"value": tot_bytes / tot_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "the step's modes, each timed on its own row sample (per_mode[*].cpu_baseline); value = "
+                      "bf16 bytes of one row through every mode / the summed per-row times"}
+    return step, per
+
+
+def mse_on_device(W, codes, scales, alpha, chunk_rows=1024) -> float:
+    """(1/N) sum (x - q * fl(alpha * Delta))^2 in double, on the device (a
+    statistic of the outputs, computed outside the timed region)."""
+    import torch
+    mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0],
+                        dtype=torch.float64, device=W.device)
+    rows, cols = W.shape
+    a32 = alpha.reshape(1).to(torch.float32)
+    acc = torch.zeros((), dtype=torch.float64, device=W.device)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        c = codes[r0:r1].to(torch.int64)
+        idx = torch.stack([c & 0xF, c >> 4], dim=-1).reshape(r1 - r0, cols)
+        q = mags[idx]
+        d = scales[r0:r1].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+        s = (a32 * d).to(torch.float64).repeat_interleave(16, dim=1)  # fl32(alpha * Delta)
+        e = W[r0:r1].to(torch.float64) - q * s
+        acc += (e * e).sum()
+    return float(acc.item()) / (rows * cols)
 
 
 # --------------------------------------------------------------------------- our arm
@@ -293,27 +358,27 @@ def run_ours(args, modes):
         gy = torch.empty((args.batch, rows), dtype=torch.float32, device=dev)
         gz = torch.empty(nv.nvfp4_swizzled_scales_bytes(rows, cols), dtype=torch.uint8, device=dev)
 
+    def slot_of(w):
+        return next(k for k in range(ncopy) if Wd[k] is w)
+
     def call(mode, w, s):
         if mode == 6:  # the slot's scales into the tensor-core layout
-            i = next(k for k in range(ncopy) if Wd[k] is w)
-            st = nv.nvfp4_swizzle_scales(dq_in[i][1].data_ptr(), rows, cols, gz.data_ptr(), s.cuda_stream)
+            st = nv.nvfp4_swizzle_scales(dq_in[slot_of(w)][1].data_ptr(), rows, cols, gz.data_ptr(), s.cuda_stream)
         elif mode == 7:  # tensor-core product of `batch` vectors with the slot's quantized tensor
-            i = next(k for k in range(ncopy) if Wd[k] is w)
-            c, sc, a = dq_in[i]
+            c, sc, a = dq_in[slot_of(w)]
             st = nv.nvfp4_gemm(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.batch,
                                gy.data_ptr(), s.cuda_stream)
         elif mode == 5:  # one-vector product with the slot's quantized tensor
-            i = next(k for k in range(ncopy) if Wd[k] is w)
-            c, sc, a = dq_in[i]
+            c, sc, a = dq_in[slot_of(w)]
             st = nv.nvfp4_gemv(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, gx.data_ptr(), args.batch,
                                gy.data_ptr(), s.cuda_stream)
         elif mode == 4:  # dequantize the slot of this W into that slot's output
-            i = next(k for k in range(ncopy) if Wd[k] is w)
+            i = slot_of(w)
             c, sc, a = dq_in[i]
             st = nv.nvfp4_dequantize(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, dq_out[i].data_ptr(),
                                      s.cuda_stream)
         else:
-            c, sc, a = outs[mode][next(k for k in range(ncopy) if Wd[k] is w)]
+            c, sc, a = outs[mode][slot_of(w)]
             st = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
                                    a.data_ptr(), s.cuda_stream)
         if st != 0:
@@ -331,7 +396,7 @@ def run_ours(args, modes):
     graphs = []
     # steps per CUDA graph: back-to-back calls chain by programmatic dependent
     # launch inside a graph, and the graph boundary costs a launch gap
-    per_graph = 8 if args.steps % 8 == 0 and not args.quick else 1
+    per_graph = 4 if args.steps % 4 == 0 and not args.quick else 1
     if not args.quick:  # ncopy CUDA graphs of `per_graph` consecutive steps each (the rotation continues)
         try:
             for i in range(ncopy):
@@ -392,10 +457,13 @@ def run_ours(args, modes):
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
            "config": {"workload": args.workload, "desc": desc, "rows": rows, "cols": cols, "modes": list(modes),
+                      "value_is": "2 bytes per element per mode (bf16 in of each quantizer, bf16 out of the "
+                                  "dequantizer) / device time of the whole step",
                       "cjso_iters": args.iters if any(2 <= m <= 3 for m in mids) else None,
                       "batch": args.batch if (5 in mids or 7 in mids) else None,
+                      "input_sha256": input_sha256(w_bits),
                       "l2": f"rotate {ncopy} input copies ({ncopy * w_bits.nbytes >> 20} MiB; L2 {l2 >> 20} MiB) "
-                            f"and {ncopy} output sets per mode",
+                            f"and {ncopy} output sets per mode: every step reads W from HBM",
                       "launch": launch, "parallelism": f"{ws} independent replica(s), one tensor per rank"},
            "gpu_launches": sum(kernels_per_call(m, args.iters) for m in mids) * args.steps, "clocks": csum}
     if args.quick:
@@ -403,16 +471,22 @@ def run_ours(args, modes):
             dist.destroy_process_group()
         return out if rank == 0 else None
 
+    # ---- the fp32 peak of this GPU, measured now (the decoupled search's roofline)
+    fp32 = nv.fp32_peak_tflops()
+    sm_mhz = csum.get("sm_mhz") or 1900.0
+    fp32["derived_at_sampled_clock"] = fp32_peak_derived(props.multi_processor_count, sm_mhz)
+    out["fp32_peak"] = fp32
+
     # ---- per mode: device throughput and per-kernel times (library CUDA events)
     per_mode = {}
     peak_hbm, peak_kind = measured_peaks()
-    sm_mhz = csum.get("sm_mhz") or 1900.0
+    tc_peak, tc_kind = measured_bf16_tflops()
     for name, m in zip(modes, mids):
-        # device time of this mode alone: graphs of 8 back-to-back calls on rotating
+        # device time of this mode alone: graphs of 4 back-to-back calls on rotating
         # copies (steady state), and graphs of one call (an isolated call's latency)
-        k = max(min(args.steps, 480), 24)
+        k = max(min(args.steps, 240), 24)
         times = {}
-        for chain in (8, 1):
+        for chain in (4, 1):
             gm = []
             if graphs:
                 for i in range(ncopy):
@@ -437,63 +511,88 @@ def run_ours(args, modes):
             torch.cuda.synchronize()
             times[chain] = e0.elapsed_time(e1) / k
             del gm
-        call_ms = times[8]
+        call_ms = times[4]
         # per-kernel breakdown from the library tracer (event-bracketed launches,
         # so each includes its launch gap)
         nv.nvfp4_profiler_reset()
         nv.nvfp4_profiler_enable(1)
-        for i in range(20):
+        for i in range(8):
             call(m, Wd[i % ncopy], stream)
         torch.cuda.synchronize()
         nv.nvfp4_profiler_enable(0)
         rep = nv.profiler_report()
-        tc_peak, tc_kind = measured_bf16_tflops()
         bound, unit, work, rule = algorithmic(m, args.iters, n, l2, args.batch, peak_hbm, tc_peak)
         if bound == "hbm":
             achieved, peak, pk = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind
-            over = "the whole call"
+            over, tkey = "the whole call", f"nvfp4_{'dequantize' if m == 4 else 'quantize'}({name})@{args.workload}"
         elif bound == "tensor":
             achieved, peak, pk = work / (call_ms / 1e3) / 1e12, tc_peak, tc_kind
-            over = "the whole call"
+            over, tkey = "the whole call", None
         else:  # the search kernel alone (its event-bracketed duration), not the CJSO sweeps before it
             kc, kt = rep["k_decoupled"]
             achieved = work / (kt / kc / 1e3) / 1e12
-            peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
-            over = "k_decoupled"
-        per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "us_per_call": call_ms * 1e3,
-                          "us_isolated_call": times[1] * 1e3,
-                          "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
-                                       "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
-                          "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
-                                                      for kn, (c, t) in rep.items()}}
-    heavy = max(per_mode, key=lambda k: per_mode[k]["us_per_call"])
-    hr = per_mode[heavy]["roofline"]
+            peak, pk = fp32["tflops"], "measured (fp32 FMA probe, this run)"
+            over, tkey = "k_decoupled", f"k_decoupled@{args.workload}"
+        pm = {"GBps_bf16_in" if m != 4 else "GBps_bf16_out": 2 * n / (call_ms / 1e3) / 1e9,
+              "us_per_call": call_ms * 1e3, "us_isolated_call": times[1] * 1e3,
+              "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                           "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
+                           "traffic": recorded_traffic(tkey) if tkey else None,
+                           "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
+              "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3} for kn, (c, t) in rep.items()}}
+        if bound == "alu":
+            pm["roofline"]["frac_of_derived_peak"] = achieved / fp32["derived_at_sampled_clock"]
+        if m < 4:  # reconstruction error of this mode's output, in double
+            c, sc, a = outs[m][0]
+            pm["mse"] = mse_on_device(Wd[0], c, sc, a)
+        per_mode[name] = pm
+    if "four_over_six" in per_mode:  # share of blocks whose FourOverSix scale is the M=4 one
+        f = outs[1][0][1]
+        mx = outs[0][0][1] if 0 in outs else nv.quantize(Wd[0], nv.MAX)[1]
+        per_mode["four_over_six"]["m4_share"] = float((f != mx).to(torch.float64).mean().item())
     out["per_mode"] = per_mode
-    out["roofline"] = {"bound": hr["bound"], "achieved": hr["achieved"], "peak": hr["peak"], "unit": hr["unit"],
-                       "frac": hr["frac"], "frac_of_nominal": hr["frac_of_nominal"],
-                       "traffic": recorded_traffic(f"nvfp4_quantize({heavy})@{args.workload}"),
-                       "kernel": (f"nvfp4_quantize({heavy}) = "
-                                  + " + ".join(per_mode[heavy]["kernels_event_bracketed"])
-                                  if hr["over"] == "the whole call" else hr["over"]),
-                       "peak_kind": hr["peak_kind"], "rule": hr["rule"],
-                       "timing": ("CUDA events on the launching stream around CUDA-graph replays of 8 calls "
-                                  "back to back on rotating inputs (per call)" if hr["over"] == "the whole call" else
-                                  "the library's CUDA events around each launch of the kernel, on its stream")}
+
+    # ---- the dominant kernel of the step: the largest share of the step's device time
+    shares = {}
+    for name, pm in per_mode.items():
+        for kn, kv in pm["kernels_event_bracketed"].items():
+            shares[(name, kn)] = kv["launches"] / 8 * kv["avg_us"]
+    (dm, dk), _ = max(shares.items(), key=lambda x: x[1])
+    pm = per_mode[dm]
+    bound, unit, work, rule = algorithmic(MODE_IDS[dm], args.iters, n, l2, args.batch, peak_hbm, tc_peak)
+    k_us = pm["kernels_event_bracketed"][dk]["avg_us"]
+    if bound == "alu" and dk == "k_decoupled":
+        achieved, peak, pk, ru = work / (k_us / 1e6) / 1e12, fp32["tflops"], "measured (fp32 FMA probe, this run)", rule
+    else:  # an HBM-bound kernel: its own bytes per launch (one read of W, or the mode's rule)
+        kb = {"k_amax_bulk": 2.0, "k_amax_partials": 2.0, "k_dequant": ONE_PASS, "k_cjso_sweep<iter>": 2.0 + 2 / 16,
+              "k_cjso_sweep<init>": 2.0 + 1 / 16}.get(dk, 2.5625)
+        achieved, peak, pk, unit = kb * n / (k_us / 1e6) / 1e9, peak_hbm, peak_kind, "GB/s"
+        bound, ru = "hbm", f"{kb} B/elem per launch"
+    total_us = sum(shares.values())
+    out["roofline"] = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                       "traffic": recorded_traffic(f"{dk}@{args.workload}"), "kernel": dk, "mode": dm,
+                       "share_of_step": shares[(dm, dk)] / total_us, "peak_kind": pk, "rule": ru,
+                       "timing": "the library's CUDA events around each launch of the kernel, on its stream "
+                                 "(average over the traced launches)"}
 
     # ---- end to end through the C ABI with pinned host buffers: every step copies
-    # its W in (H2D), quantizes it with each mode and copies every output back
-    # (D2H).  Steps are pipelined over two buffer slots and three streams, so the
-    # copies of one step overlap the kernels of its neighbours.
+    # its W in (H2D), quantizes it with each mode, dequantizes the max-rule output
+    # (when the step has dequant) and copies every output back (D2H).  Steps are
+    # pipelined over two buffer slots and three streams, so the copies of one
+    # step overlap the kernels of its neighbours.
     W_pin = W_host.pin_memory()
     qmids = [m for m in mids if m < 4]
+    with_dq = 4 in mids
     slots = []
     for _ in range(2):
         o = {m: tuple(torch.empty_like(t) for t in outs[m][0]) for m in qmids}
         ho = {m: tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[m][0]) for m in qmids}
-        slots.append({"W": torch.empty_like(Wd[0]), "outs": o, "host": ho,
+        dq = (torch.empty((rows, cols), dtype=torch.bfloat16, device=dev),
+              torch.empty((rows, cols), dtype=torch.bfloat16).pin_memory()) if with_dq else None
+        slots.append({"W": torch.empty_like(Wd[0]), "outs": o, "host": ho, "dq": dq,
                       "h2d": torch.cuda.Event(), "comp": torch.cuda.Event(), "d2h": torch.cuda.Event()})
     s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dq_src = qmids[0] if qmids else None
 
     def qcall(mode, w, o, st):
         c, sc, a = o
@@ -512,22 +611,30 @@ def run_ours(args, modes):
         stream.wait_event(sl["d2h"])  # the slot's outputs have been copied out
         for m in qmids:
             qcall(m, sl["W"], sl["outs"][m], stream)
+        if with_dq and dq_src is not None:
+            c, sc, a = sl["outs"][dq_src]
+            r = nv.nvfp4_dequantize(c.data_ptr(), sc.data_ptr(), a.data_ptr(), rows, cols, sl["dq"][0].data_ptr(),
+                                    stream.cuda_stream)
+            if r != 0:
+                raise RuntimeError(f"nvfp4_dequantize: {nv.nvfp4_status_string(r)}")
         sl["comp"].record(stream)
         s_d2h.wait_event(sl["comp"])
         with torch.cuda.stream(s_d2h):
             for m in qmids:
                 for dst, src in zip(sl["host"][m], sl["outs"][m]):
                     dst.copy_(src, non_blocking=True)
+            if with_dq:
+                sl["dq"][1].copy_(sl["dq"][0], non_blocking=True)
         sl["d2h"].record(s_d2h)
 
-    for i in range(4):
+    for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    k_e2e = max(min(args.steps // 4, 200), 6)
+    k_e2e = max(min(args.steps, 200), 6)
     e0.record(stream)
     s_h2d.wait_stream(stream)
     for i in range(k_e2e):
@@ -537,15 +644,18 @@ def run_ours(args, modes):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev, ws)
     d2h = sum(t.numel() * t.element_size() for m in slots[0]["host"] for t in slots[0]["host"][m])
-    out["e2e"] = {"value": job_gbs(ws, len(qmids) * 2 * n, k_e2e, e2e_ms), "unit": "GB/s",
-                  "modes": [m for m in modes if m not in CONSUMERS],
-                  "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h, "steps": k_e2e,
-                  "pipelining": "2 buffer slots; H2D, kernels and D2H on three streams"}
+    if with_dq:
+        d2h += 2 * n
+    out["e2e"] = {"value": job_gbs(ws, bytes_per_step, k_e2e, e2e_ms), "unit": "GB/s",
+                  "modes": list(modes), "h2d_bytes_per_step": w_bits.nbytes, "d2h_bytes_per_step": d2h,
+                  "steps": k_e2e, "pipelining": "2 buffer slots; H2D, kernels and D2H on three streams"}
 
     if rank == 0 and ws == 1:
-        rows_cap = None if n <= (1 << 24) else max(16, (1 << 22) // cols)
-        out["cpu_baseline"] = oracle_cpu_baseline(w_bits, [m for m in modes if m not in CONSUMERS], args.iters,
-                                                  max_rows=rows_cap)
+        step_cpu, per_cpu = oracle_cpu_baseline(w_bits, [m for m in modes if m in HOT_PATH], args.iters)
+        out["cpu_baseline"] = step_cpu
+        for m, v in per_cpu.items():
+            per_mode[m]["cpu_baseline"] = v
+    del Wd, outs, slots
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -575,7 +685,7 @@ def model_tensors(dev, layers=32):
     return shapes, Ws
 
 
-def run_model(args, modes):
+def run_model(args, modes, fp32=None, steps=None):
     import torch
 
     import nvfp4_block_scale_gb300 as nv
@@ -625,6 +735,7 @@ def run_model(args, modes):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    steps = args.steps if steps is None else steps
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -632,19 +743,20 @@ def run_model(args, modes):
     clocks = ClockSampler(local)
     for attempt in range(2):
         clocks.start()
-        ms = event_ms(gstep.replay, args.steps)
+        ms = event_ms(gstep.replay, steps)
         clocks.stop()
         csum = clocks.summary()
         if not (set(csum.get("reasons", [])) & BAD_REASONS):
             break
         csum["remeasured"] = True
-    value = len(mids) * 2 * n * args.steps / (ms / 1e3) / 1e9
+    del gstep
+    value = len(mids) * 2 * n * steps / (ms / 1e3) / 1e9
     launches = 0
     for m in mids:
         launches += 2 * math.ceil(len(Ws) / nv.NVFP4_GROUP_MAX) if m in (0, 1) else \
             len(Ws) * kernels_per_call(m, args.iters)
-    out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+    out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps,
+           "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
            "config": {"workload": MODEL, "desc": MODEL_DESC, "layers": args.layers, "tensors": len(Ws),
                       "elements": n,
@@ -652,30 +764,34 @@ def run_model(args, modes):
                       "l2": f"inputs {2 * n >> 30} GiB, larger than L2 ({l2 >> 20} MiB)",
                       "launch": "cuda_graph of nvfp4_quantize_grouped per mode",
                       "parallelism": "1 GPU"},
-           "gpu_launches": launches * args.steps, "clocks": csum}
+           "gpu_launches": launches * steps, "clocks": csum}
     if args.quick:
         return out
 
     peak_hbm, peak_kind = measured_peaks()
-    sm_mhz = csum.get("sm_mhz") or 1900.0
+    if fp32 is None:
+        fp32 = nv.fp32_peak_tflops()
     per_mode = {}
     for name, m in zip(qmodes, mids):
         k = 3 if m >= 2 else 20
         gm = graph_of(lambda: grouped(m))
         call_ms = event_ms(gm.replay, k) / k
+        del gm
         gp = graph_of(lambda: per_tensor(m))
         per_tensor_ms = event_ms(gp.replay, k) / k
-        del gm, gp
+        del gp
         nv.nvfp4_profiler_reset()
         nv.nvfp4_profiler_enable(1)
         grouped(m)
         torch.cuda.synchronize()
         nv.nvfp4_profiler_enable(0)
         rep = nv.profiler_report()
+        tkey = None
         if m in (0, 1):  # per tensor: one HBM read when it fits in half of L2, else two
             work = sum((ONE_PASS if 2 * x <= l2 // 2 else TWO_PASS) * x for x in ns)
             achieved, peak, pk, unit, bound = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind, "GB/s", "hbm"
             rule, over = "2.5625 B/elem for tensors <= L2/2, 4.5625 above", "the whole call"
+            tkey = f"nvfp4_quantize_grouped({name})@{MODEL}"
         elif m == 2:
             work = sum(((args.iters + 2) * 2 + 0.5625) * x for x in ns)
             achieved, peak, pk, unit, bound = work / (call_ms / 1e3) / 1e9, peak_hbm, peak_kind, "GB/s", "hbm"
@@ -684,21 +800,28 @@ def run_model(args, modes):
             kc, kt = rep["k_decoupled"]
             work = DECOUPLED_FLOPS * n
             achieved = work / (kt / 1e3) / 1e12
-            peak, pk = fp32_peak_tflops(props.multi_processor_count, sm_mhz), f"derived at {sm_mhz:.0f} MHz"
-            unit, bound, over = "TFLOP/s", "alu", "k_decoupled (all tensors)"
+            peak, pk = fp32["tflops"], "measured (fp32 FMA probe, this run)"
+            unit, bound, over = "TFLOP/s", "alu", "k_decoupled (all tensors; sum of their durations)"
             rule = "505 fp32 flop/elem (101 candidates x [1 FMUL + 2 FMA])"
-        per_mode[name] = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "ms_per_call": call_ms,
-                          "per_tensor_calls_ms": per_tensor_ms,
-                          "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                                       "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
-                                       "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
-                          "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
-                                                      for kn, (c, t) in rep.items()}}
+        pm = {"GBps_bf16_in": 2 * n / (call_ms / 1e3) / 1e9, "ms_per_call": call_ms,
+              "per_tensor_calls_ms": per_tensor_ms,
+              "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                           "frac": achieved / peak, "peak_kind": pk, "rule": rule, "over": over,
+                           "traffic": recorded_traffic(tkey) if tkey else None,
+                           "frac_of_nominal": (achieved / NOMINAL_HBM_GBS if bound == "hbm" else None)},
+              "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3}
+                                          for kn, (c, t) in rep.items()}}
+        # reconstruction error and M=4 share over the stack (statistics of the outputs)
+        pm["mse"] = sum(mse_on_device(W, *o) * W.numel() for W, o in zip(Ws, outs)) / n
+        if m == 1:
+            mx = [nv.quantize(W, nv.MAX)[1] for W in Ws[:7]]
+            nb = sum(o[1].numel() for o in outs[:7])
+            pm["m4_share_layer0"] = sum(float((o[1] != x).sum().item()) for o, x in zip(outs[:7], mx)) / nb
+        per_mode[name] = pm
     heavy = max(per_mode, key=lambda x: per_mode[x]["ms_per_call"])
     hr = per_mode[heavy]["roofline"]
     out["per_mode"] = per_mode
-    out["roofline"] = dict(hr, traffic=recorded_traffic(f"nvfp4_quantize_grouped({heavy})@{MODEL}"),
-                           kernel=f"nvfp4_quantize_grouped({heavy})")
+    out["roofline"] = dict(hr, kernel=f"nvfp4_quantize_grouped({heavy})")
 
     # end to end over layer 0 (7 tensors) through the C ABI with pinned host buffers
     lay = list(range(7))
@@ -725,9 +848,13 @@ def run_model(args, modes):
                   "h2d_bytes_per_step": 2 * n_lay,
                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for ho in host_o for t in ho),
                   "steps": k_e2e}
-    w0 = Ws[0][:64].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    out["cpu_baseline"] = oracle_cpu_baseline(w0, qmodes, args.iters)
-    out["cpu_baseline"]["sample"] += " (layer 0 q_proj)"
+    w0 = Ws[0][:512].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    step_cpu, per_cpu = oracle_cpu_baseline(w0, qmodes, args.iters, min_seconds=3.0)
+    out["cpu_baseline"] = dict(step_cpu, sample=step_cpu["sample"] + " (layer 0 q_proj)")
+    for m, v in per_cpu.items():
+        per_mode[m]["cpu_baseline"] = dict(v, sample=v["sample"] + " (layer 0 q_proj)")
+    del Ws, outs
+    torch.cuda.empty_cache()
     return out
 
 
@@ -743,17 +870,24 @@ def run_reference(args, modes):
     else:
         make, desc, _ = WORKLOADS[args.workload]
         w_bits = make(0)
-    rows = max(16, min(w_bits.shape[0], (1 << 21) // w_bits.shape[1]))
-    if any(m == "cjso_decoupled" for m in modes):
-        rows = max(16, min(rows, (1 << 18) // w_bits.shape[1]))
-    sample = w_bits[:rows]  # bounded per-step sample of the workload
     threads = os.cpu_count() or 1
-
-    qmodes = [m for m in modes if m not in CONSUMERS]
+    qmodes = [m for m in modes if m not in CONSUMERS or m == "dequant"]
+    # a bounded per-step sample: each mode on its own first rows of W, about a
+    # second of oracle work per mode on 16 host cores
+    samples = {m: np.ascontiguousarray(w_bits[:max(16, oracle_rows(m, w_bits.shape[1], w_bits.shape[0]) // 4)])
+               for m in qmodes}
+    deq_in = {}
+    if "dequant" in samples:
+        s = samples["dequant"]
+        deq_in = oracle.quantize(s, oracle.MAX, 0, threads=threads)
 
     def step():
         for m in qmodes:
-            oracle.quantize(sample, MODE_IDS[m], args.iters, threads=threads)
+            s = samples[m]
+            if m == "dequant":
+                oracle.dequantize(*deq_in, s.shape[0], s.shape[1])
+            else:
+                oracle.quantize(s, MODE_IDS[m], args.iters, threads=threads)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -761,15 +895,19 @@ def run_reference(args, modes):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = len(qmodes) * sample.nbytes * args.steps / el / 1e9
-    sdesc = (f"C oracle, {threads} host threads, rows 0..{rows - 1} of the {w_bits.shape[0]}x{w_bits.shape[1]} "
-             f"tensor per step, {'+'.join(modes)}")
+    # same definition as our arm's value: 2 bytes per element per mode over the step
+    # time, with each mode's share of a step scaled from its sample to one row
+    per_row_s = sum(el / args.steps / samples[m].shape[0] for m in qmodes)
+    value = len(qmodes) * 2 * w_bits.shape[1] / per_row_s / 1e9
+    sdesc = (f"C oracle, {threads} host threads, per step each mode on its own first rows of the "
+             f"{w_bits.shape[0]}x{w_bits.shape[1]} tensor ("
+             + ", ".join(f"{m}: {samples[m].shape[0]}" for m in qmodes) + " rows)")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
             "config": {"workload": args.workload, "desc": desc, "rows": int(w_bits.shape[0]),
-                       "cols": int(w_bits.shape[1]), "modes": list(modes)},
+                       "cols": int(w_bits.shape[1]), "modes": list(modes), "input_sha256": input_sha256(w_bits)},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sdesc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -777,14 +915,16 @@ def run_reference(args, modes):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + [MODEL])
     ap.add_argument("--modes", default=None, help="comma list of " + ",".join(MODE_IDS))
     ap.add_argument("--iters", type=int, default=5, help="CJSO iterations")
     ap.add_argument("--layers", type=int, default=32, help=f"layers of the {MODEL} stack (1..32)")
+    ap.add_argument("--stack-steps", type=int, default=4, help=f"timed steps of the {MODEL} record")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors of the gemv (1..8) and gemm (1..256) modes")
+    ap.add_argument("--no-stack", action="store_true", help=f"skip the {MODEL} record of the headline run")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
@@ -799,6 +939,11 @@ def main():
         out = run_model(args, modes)
     else:
         out = run_ours(args, modes)
+        ws, rank, _ = dist_env()
+        if (out is not None and ws == 1 and not args.quick and not args.no_stack and args.workload == HEADLINE
+                and args.modes is None):
+            out["workloads"] = {MODEL: run_model(args, ("four_over_six", "cjso_decoupled"), out.get("fp32_peak"),
+                                                  steps=args.stack_steps)}
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -284,6 +284,21 @@ int nvfp4_profiler_reset(void);
 int nvfp4_profiler_kinds(void);
 int nvfp4_profiler_get(int index, char *name, int name_len, int64_t *launches, double *total_ms);
 
+/*
+ * nvfp4_ffma_probe -- fp32 fused multiply-add throughput probe: launches one
+ *   kernel on `stream` in which every resident thread of every SM runs
+ *   independent FMA chains for `rounds` rounds (scalar fma.rn.f32 when
+ *   packed == 0, packed fma.rn.f32x2 when packed == 1).  The caller times the
+ *   launch (CUDA events on `stream`); 2 x *fmas / seconds is the fp32 peak at
+ *   the clock the launch ran at.  (No counterpart on the method's pages: it
+ *   gives the fp32-bound scale search its roofline.)
+ * Arguments: packed 0 or 1; rounds 1..2^32; sink (device, 4-byte aligned,
+ *   sink_floats floats, overwritten; at least 2048 x the SM count is always
+ *   enough); fmas (host, written: FMAs the launch performs).
+ */
+int nvfp4_ffma_probe(int packed, int64_t rounds, float *sink, int64_t sink_floats, int64_t *fmas,
+                     cudaStream_t stream);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char *nvfp4_status_string(int status);
 

@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_profiler_get.argtypes = [ci, ctypes.c_char_p, ci, ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_double)]
     L.nvfp4_profiler_get.restype = ci
+    L.nvfp4_ffma_probe.argtypes = [ci, i64, vp, i64, ctypes.POINTER(ctypes.c_int64), vp]
+    L.nvfp4_ffma_probe.restype = ci
     L.nvfp4_status_string.argtypes = [ci]
     L.nvfp4_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -132,6 +134,11 @@ def nvfp4_encode_e4m3(v, n, out, stream) -> int:
     return load().nvfp4_encode_e4m3(v, n, out, stream)
 
 
+def nvfp4_ffma_probe(packed, rounds, sink, sink_floats, fmas, stream) -> int:
+    """fp32 FMA throughput probe (instrumentation); `fmas` is a ctypes int64 pointer."""
+    return load().nvfp4_ffma_probe(packed, rounds, sink, sink_floats, fmas, stream)
+
+
 def nvfp4_status_string(status: int) -> str:
     return load().nvfp4_status_string(int(status)).decode()
 
@@ -168,6 +175,36 @@ def profiler_report() -> dict:
 
 
 # ------------------------------------------------------------ torch helpers
+
+def fp32_peak_tflops(seconds: float = 0.05, stream=None) -> dict:
+    """Measured fp32 FMA peak of the current device (TFLOP/s): the probe
+    kernel, scalar and packed, each timed with CUDA events after a warm-up
+    launch; the larger of the two is the peak."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.empty(2048 * sms, dtype=torch.float32, device="cuda")
+    res = {}
+    for packed in (0, 1):
+        fmas = ctypes.c_int64()
+        rounds = 1 << 12
+        for _ in range(12):  # grow until one launch takes about `seconds`
+            _check(nvfp4_ffma_probe(packed, rounds, sink.data_ptr(), sink.numel(), ctypes.byref(fmas), s.cuda_stream),
+                   "nvfp4_ffma_probe")
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            _check(nvfp4_ffma_probe(packed, rounds, sink.data_ptr(), sink.numel(), ctypes.byref(fmas), s.cuda_stream),
+                   "nvfp4_ffma_probe")
+            e1.record(s)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            if ms >= seconds * 1e3 or rounds >= (1 << 30):
+                break
+            rounds = min(1 << 30, rounds * max(2, int(seconds * 1e3 / max(ms, 1e-3))))
+        res["packed" if packed else "scalar"] = 2.0 * fmas.value / (ms / 1e3) / 1e12
+    res["tflops"] = max(res["scalar"], res["packed"])
+    return res
+
 
 def _stream_ptr(stream):
     import torch

@@ -76,6 +76,7 @@ int device_info(DevInfo **out) {
       d.status = NVFP4_ERR_UNSUPPORTED_DEVICE;
     } else {
       e = prepare_decoupled_kernel();
+      if (e == cudaSuccess) e = prepare_quant_kernels();
       if (e != cudaSuccess) return map_cuda(e);
       for (int k = 0; k < kKernCount; ++k) d.occ[k] = max_active_ctas(k);
       e = prepare_gemv_kernels();
@@ -217,24 +218,6 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
-  const int64_t dec_full = int64_t(d->sms) * d->occ[kKernDecoupled];  // 1024-thread CTAs
-  // decoupled search: 1, 2 or 4 lanes per block, whichever finishes first in
-  // candidate evaluations per thread (blocks per thread x candidates per lane)
-  int g_dec = 1, split_dec = 1;
-  {
-    int64_t best = INT64_MAX;
-    for (int sp = 1; sp <= 4; sp *= 2) {
-      const int64_t need = std::max<int64_t>(1, (B * sp + 1023) / 1024);
-      const int64_t grid = std::min(need, dec_full);
-      const int64_t cost = ((B * sp + grid * 1024 - 1) / (grid * 1024)) * ((101 + sp - 1) / sp);
-      if (cost < best) {
-        best = cost;
-        g_dec = (int)grid;
-        split_dec = sp;
-      }
-    }
-  }
-
   // scratch: amax partials | 2 x CJSO partial sums | alpha history
   const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);
   const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 16, 256);
@@ -270,7 +253,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
     }
     if (e == cudaSuccess && !plain) {
       TraceScope tr(kTrDecoupled, stream);
-      e = launch_decoupled(W, B, hist, T, scales, codes, g_dec, split_dec, stream);
+      e = launch_decoupled(W, B, hist, T, scales, codes, d->sms, stream);
     }
   }
   // The scratch goes back to the pool in stream order, after the last kernel.
@@ -499,6 +482,21 @@ int nvfp4_encode_e4m3(const float *v, int64_t n, uint8_t *out, cudaStream_t stre
   if (n == 0) return NVFP4_OK;
   TraceScope tr(kTrEncode, stream);
   return map_cuda(launch_encode_e4m3(v, n, out, grid_for(*d, kKernDequant, n), stream));
+}
+
+int nvfp4_ffma_probe(int packed, int64_t rounds, float *sink, int64_t sink_floats, int64_t *fmas,
+                     cudaStream_t stream) {
+  if ((packed != 0 && packed != 1) || rounds < 1 || rounds > (int64_t(1) << 32) || !sink || !fmas)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(sink, 4)) return NVFP4_ERR_MISALIGNED;
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  const int grid = d->sms * ffma_probe_occupancy(packed);
+  const int64_t threads = int64_t(grid) * ffma_probe_threads();
+  if (sink_floats < threads) return NVFP4_ERR_INVALID_ARG;
+  *fmas = threads * ffma_probe_fmas_per_thread(packed, rounds);
+  return map_cuda(launch_ffma_probe(packed, rounds, grid, sink, stream));
 }
 
 int nvfp4_profiler_enable(int on) {

@@ -1,0 +1,342 @@
+// nvfp4_decoupled.cu -- the decoupled quantization / dequantization scale
+// search of [SOAR-DEC], as an event-driven scan over the 101 candidates.
+//
+// Citation keys (page title, part of the page):
+//   [SOAR-Q]   "SOAR: Scale Optimization for Accurate Reconstruction in NVFP4
+//              Quantization": NVFP4 quantizer equation (piecewise FP4
+//              rounding of X / (alpha * Delta)).
+//   [SOAR-DEC] same page: decoupled objective (Delta^q real, Delta^d FP8)
+//              and its search: Delta^q = Delta^d0 * {0.50, 0.51, ..., 1.50},
+//              Delta^d limited to the two nearest E4M3 values, the pair of
+//              least reconstruction error kept.
+//
+// What is computed (per 16-element block, alpha and Delta^d0 from CJSO):
+// for k = 0..100, sq_k = fl(alpha * fl(Delta^d0 * m_k)) with m_k =
+// fl32((50 + k) / 100); the codes Q_k = e2m1(fl(|x| / sq_k)); P_k = sum |x| q,
+// R_k = sum q^2 (exact); for the two E4M3 values lo_k <= fl(Delta^d0 m_k) <=
+// hi_k, g = fl(sd * fma(sd, R_k, -2 P_k)) with sd = fl(alpha * Delta^d); the
+// first strict minimum of g in the order (k ascending, lo before hi) wins.
+//
+// How: sq_k grows with k, so every element's code only steps down as k grows,
+// at most 4 times over the range (the quotient spans a factor of 3, and four
+// E2M1 decision points at most fit in a factor of 3).  Element x crosses the
+// decision point b between codes i and i+1 at about kappa = 100 |x| / (b
+// s50) - 50 (s50 = fl(alpha Delta^d0)); kappa computed in fp32 is within
+// 8e-5 of the true crossing (error bound below), so K = ceil(kappa) is the
+// first k with the lower code unless kappa lies within 2^-12 of an integer
+// (never seen on the benchmark tensors; such a block takes the plain loop
+// below).  Each crossing
+// adds its exact change of P and R to a per-thread shared-memory slot at K
+// (P as an integer multiple of 2^(-E-1), R as quarters, packed in one word);
+// a scan then visits only the k where P, R or the E4M3 bracket changes and
+// evaluates the two candidates there.  Between visited k, every candidate's
+// g equals the previous one bit for bit, and a later equal g never wins
+// under the strict comparison, so the winner is that of the full 202-
+// candidate loop.
+//
+// Error bound of kappa: sq_k = alpha Delta^d0 (50+k)/100 (1 + theta), |theta|
+// <= 3 u (u = 2^-24: m_k, the product with Delta^d0, the product with
+// alpha), s50 carries one more u, and the code changes where fl(|x|/sq_k)
+// crosses b, i.e. where |x|/sq_k is within u b of b; the true crossing k is
+// 100 V / b (1 + lambda) - 50 with V = |x| / s50, |lambda| <= 5u, i.e. within
+// 150 * 5u = 4.5e-5.  kappa = fl(fl(|x| fl(1/s50)) * fl(100/b) - 50) carries
+// at most 3u relative on the product (<= 150) and one rounding of a value <=
+// 100: 3.3e-5.  Total < 8e-5, against the 2^-12 = 2.4e-4 margin.
+//
+// Exactness of P: with 2^E chosen so that max|x| 2^E < 2^15, X = |x| 2^E is
+// an integer for every element of magnitude >= 2^(7-E); every element whose
+// code is nonzero for some candidate has |x| > s50 / 8, so s50 2^E >= 1025
+// makes all of them exact, and P = sum X 2q * 2^(-E-1) is exact (sum < 2^23).
+// Blocks outside that range (a block maximum far above its scale) take the
+// plain per-candidate loop.
+//
+// SIMT shape: one block per thread; the crossing loops run a fixed 4 steps
+// under predicates and the warp reconverges (__syncwarp) after each phase,
+// so the 32 lanes of a warp stay together; every lane of a warp runs the
+// same number of block iterations (lanes past the last block idle inside).
+#include <cuda_runtime.h>
+
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+constexpr int kDecThreads = 512;
+constexpr int kDecK = 101;
+constexpr int kSlotK = 100;  // k = 1..100 (k = 0 is the start state)
+constexpr float kAmbig = 0x1p-12f;
+
+// Dynamic shared memory: per-thread event slots and breakpoint masks, then
+// the per-CTA tables.
+constexpr size_t kOffMask = (size_t)kSlotK * kDecThreads * 4;
+constexpr size_t kOffLohi = kOffMask + (size_t)4 * kDecThreads * 4;
+constexpr size_t kOffS = kOffLohi + 128 * 4 * 4;
+constexpr size_t kOffR = kOffS + 128 * 4;
+constexpr size_t kOffEv = kOffR + 128 * 4;
+constexpr size_t kOffM = kOffEv + 128 * 4;
+constexpr size_t kOffLo = kOffM + 112 * 4;
+constexpr size_t kDecSmem = kOffLo + 128 * kDecK;
+static_assert(kDecSmem <= 232448, "dynamic shared memory of one CTA");
+
+// fl(100 / b) for the E2M1 decision points b = 0.25, 0.75, 1.25, 1.75, 2.5,
+// 3.5, 5 (b_i lies between magnitude codes i and i + 1).
+__constant__ float kHundredOverB[7] = {(float)(100.0 / 0.25), (float)(100.0 / 0.75), (float)(100.0 / 1.25),
+                                       (float)(100.0 / 1.75), (float)(100.0 / 2.5),  (float)(100.0 / 3.5),
+                                       (float)(100.0 / 5.0)};
+
+// Byte lookups (prmt on two words holding an 8-byte table).
+__device__ __forceinline__ uint32_t lut8(uint32_t lo4, uint32_t hi4, uint32_t idx) {
+  return __byte_perm(lo4, hi4, idx & 7u) & 0xFFu;
+}
+// 2q and 4q^2 of a magnitude code: {0,1,2,3,4,6,8,12}, {0,1,4,9,16,36,64,144}
+__device__ __forceinline__ uint32_t two_q(uint32_t c) { return lut8(0x03020100u, 0x0C080604u, c); }
+__device__ __forceinline__ uint32_t four_q2(uint32_t c) { return lut8(0x09040100u, 0x90402410u, c); }
+// Crossing decision point i (code i+1 -> i): 2(q_{i+1} - q_i) = 1,1,1,1,2,2,4 as
+// a shift, and 4(q_{i+1}^2 - q_i^2) = 1,3,5,7,20,28,80.
+__device__ __forceinline__ uint32_t step_shift(uint32_t i) { return lut8(0x00000000u, 0x00020101u, i); }
+__device__ __forceinline__ uint32_t step_r4(uint32_t i) { return lut8(0x07050301u, 0x00501C14u, i); }
+
+// E4M3 codes bracketing dq >= 0: lo = largest with value <= dq, hi = smallest
+// with value >= dq (448 above 448), packed as lo | (hi != lo) << 7.
+__device__ __forceinline__ uint32_t bracket_byte(float dq, const float *ev_tab) {
+  const uint32_t n = e4m3_code(dq);  // nearest
+  const float vn = ev_tab[n];
+  const uint32_t lo = vn > dq ? n - 1u : n;
+  const uint32_t hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
+  return lo | ((hi != lo ? 1u : 0u) << 7);
+}
+
+__device__ __forceinline__ float elem(const Block16 &blk, int j) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(blk.x[j >> 1]));
+  return (j & 1) ? hi : lo;
+}
+
+// The plain search for blocks outside the exact-integer range: every
+// candidate's P, R from its own quotients (the block's scaled f16 image for P).
+__device__ __noinline__ int search_plain(uint4 a0, uint4 a1, float alpha, float ev0, uint32_t d0,
+                                         const float *s_tab, const float *m_tab, const uint8_t *lo_tab) {
+  Block16 blk;
+  const uint32_t am = unpack16(a0, a1, blk);
+  BlockH16 bh;
+  make_h16(blk, am, bh);
+  float best_g = __int_as_float(0x7F800000);
+  int best_i = 0;
+  for (int k = 0; k < kDecK; ++k) {
+    const float sq = __fmul_rn(alpha, __fmul_rn(ev0, m_tab[k]));
+    const float r = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
+    float m2P, R;
+    block_sums_h(blk, bh, sq, r, m2P, R);
+    const uint32_t lb = lo_tab[d0 * kDecK + k];
+    const uint32_t lo = lb & 0x7Fu, hi = lo + (lb >> 7);
+    const float glo = cand_err_m2p(s_tab[lo], m2P, R);
+    const float ghi = cand_err_m2p(s_tab[hi], m2P, R);
+    if (glo < best_g) { best_g = glo; best_i = 2 * k; }
+    if (ghi < best_g) { best_g = ghi; best_i = 2 * k + 1; }
+  }
+  return best_i;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
+                                                              const float *__restrict__ alpha_hist, int t,
+                                                              uint8_t *__restrict__ scales,
+                                                              uint32_t *__restrict__ codes32) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint32_t *slot = reinterpret_cast<uint32_t *>(dsm);            // [k - 1][thread]
+  uint32_t *mask = reinterpret_cast<uint32_t *>(dsm + kOffMask);  // [word][thread]
+  uint32_t *lohi = reinterpret_cast<uint32_t *>(dsm + kOffLohi);  // [Delta^d0 code][word]
+  float *s_tab = reinterpret_cast<float *>(dsm + kOffS);          // fl(alpha * value)
+  float *r_tab = reinterpret_cast<float *>(dsm + kOffR);          // its IEEE reciprocal
+  float *ev_tab = reinterpret_cast<float *>(dsm + kOffEv);        // E4M3 values
+  float *m_tab = reinterpret_cast<float *>(dsm + kOffM);          // m_k (101), then fl(100 / b_i) (7)
+  uint8_t *lo_tab = dsm + kOffLo;                                 // [Delta^d0 code][k] bracket byte
+  float *h_tab = m_tab + kDecK;
+  const int tid = threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * kDecThreads;
+  const int64_t warp_first = (int64_t)blockIdx.x * kDecThreads + (tid & ~31);
+  int64_t b = (int64_t)blockIdx.x * kDecThreads + tid;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
+
+  // alpha-independent set-up, overlapping the previous kernel's tail
+  for (int k = 0; k < kSlotK; ++k) slot[k * kDecThreads + tid] = 0u;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) mask[w * kDecThreads + tid] = 0u;
+  if (tid < 128) ev_tab[tid] = e4m3_value(tid);
+  if (tid < kDecK) m_tab[tid] = __double2float_rn(__ddiv_rn((double)(50 + tid), 100.0));  // m_k
+  if (tid < 7) h_tab[tid] = kHundredOverB[tid];
+  __syncthreads();
+  for (int e = tid; e < 128 * kDecK; e += kDecThreads) {
+    const int c = e / kDecK, k = e - c * kDecK;
+    lo_tab[e] = (uint8_t)bracket_byte(__fmul_rn(ev_tab[c], m_tab[k]), ev_tab);
+  }
+  __syncthreads();
+  if (tid < 128) {  // the k where the bracket (lo, hi) of Delta^d0 = code tid changes, and k = 0
+    uint32_t m0 = 1u, m1 = 0u, m2 = 0u, m3 = 0u;
+    uint32_t prev = lo_tab[tid * kDecK];
+    for (int k = 1; k < kDecK; ++k) {
+      const uint32_t cur = lo_tab[tid * kDecK + k];
+      const uint32_t bit = cur != prev ? 1u << (k & 31) : 0u;
+      m0 |= (k >> 5) == 0 ? bit : 0u;
+      m1 |= (k >> 5) == 1 ? bit : 0u;
+      m2 |= (k >> 5) == 2 ? bit : 0u;
+      m3 |= (k >> 5) == 3 ? bit : 0u;
+      prev = cur;
+    }
+    lohi[tid * 4 + 0] = m0;
+    lohi[tid * 4 + 1] = m1;
+    lohi[tid * 4 + 2] = m2;
+    lohi[tid * 4 + 3] = m3;
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  const float alpha = alpha_hist[t];
+  if (tid < 128) {
+    const float s = __fmul_rn(alpha, ev_tab[tid]);
+    s_tab[tid] = s;
+    r_tab[tid] = s > 0.0f ? __frcp_rn(s) : 0.0f;
+  }
+  __syncthreads();
+
+  uint32_t *my_slot = slot + tid;
+  uint32_t *my_mask = mask + tid;
+  // warp-uniform trip count: wf is the warp's first block of the iteration
+  for (int64_t wf = warp_first; wf < B; wf += stride, b += stride) {
+    const bool live = b < B;
+    const int64_t nb = b + stride;
+    const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
+    Block16 blk;
+    const uint32_t am = unpack16(a0, a1, blk);
+    const uint32_t d0 = live ? scales[b] : 0u;
+    const float s50 = s_tab[d0];
+    const float r50 = r_tab[d0];
+    const float ev0 = ev_tab[d0];
+    const int e_a = (int)(am >> 7);  // biased exponent of the block maximum
+    const float sc = __uint_as_float((uint32_t)(268 - min(max(e_a, 15), 254)) << 23);  // 2^E, E = 141 - e_a
+    // 0: zero scale (sign-only codes); 1: event scan; 2: plain loop
+    int path = !(s50 > 0.0f) ? 0 : ((e_a >= 15 && __fmul_rn(s50, sc) >= 1025.0f) ? 1 : 2);
+    float P_unused, R_unused;
+    int best_i = 0;
+    if (path == 1) {
+      const float nsc = -__uint_as_float((uint32_t)(max(e_a, 15) - 14) << 23);  // -2^-E
+      // exact magnitude codes at k = 0 (sq_0 = s50 / 2, its reciprocal 2 / s50)
+      uint32_t q0, q1;
+      quant16<false>(blk, __fmul_rn(s50, 0.5f), __fmul_rn(r50, 2.0f), q0, q1, P_unused, R_unused);
+      q0 &= 0x77777777u;
+      q1 &= 0x77777777u;
+      int P = 0, R4 = 0;  // P = P_int * 2^(-E-1), R = R4 / 4
+      bool amb = false;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float xa = fabsf(elem(blk, j));
+        const uint32_t c = ((j < 8 ? q0 : q1) >> (4 * (j & 7))) & 7u;
+        const uint32_t X = __float2uint_rz(__fmul_rn(xa, sc));
+        P += (int)(X * two_q(c));
+        R4 += (int)four_q2(c);
+        const float v = __fmul_rn(xa, r50);
+        bool go = true;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {  // the element's crossings, in k order: decision points c-1, c-2, ...
+          const int i = (int)c - 1 - st;
+          go = go && i >= 0;
+          const int ii = max(i, 0);
+          const float kap = __fmaf_rn(v, h_tab[ii], -50.0f);
+          const float n = rintf(kap);
+          // within kAmbig of an integer n in 1..100 the crossing may be at n or n + 1
+          // (near 0 it is at 1: the code at k = 0 is known)
+          amb = amb || (go && n >= 1.0f && n <= 100.0f && fabsf(__fsub_rn(kap, n)) < kAmbig);
+          const int K = max((int)ceilf(kap), 1);
+          go = go && K <= kSlotK;
+          if (go) {
+            atomicAdd(my_slot + (K - 1) * kDecThreads, (X << (11 + step_shift(ii))) + step_r4(ii));
+            atomicOr(my_mask + (K >> 5) * kDecThreads, 1u << (K & 31));
+          }
+        }
+      }
+      if (amb) {  // a crossing too close to an integer k: undo the events, take the plain loop
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t bits = my_mask[w * kDecThreads];
+          my_mask[w * kDecThreads] = 0u;
+          while (bits) {
+            const int k = 32 * w + __ffs(bits) - 1;
+            bits &= bits - 1u;
+            my_slot[(k - 1) * kDecThreads] = 0u;
+          }
+        }
+        path = 2;
+      } else {
+        // scan the breakpoints in k order
+        float best_g = __int_as_float(0x7F800000);
+        const uint32_t *lm = lohi + d0 * 4;
+        const uint8_t *lrow = lo_tab + d0 * kDecK;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t bits = lm[w] | my_mask[w * kDecThreads];
+          my_mask[w * kDecThreads] = 0u;
+          while (bits) {
+            const int k = 32 * w + __ffs(bits) - 1;
+            bits &= bits - 1u;
+            const int ks = max(k - 1, 0);
+            const uint32_t ev = k > 0 ? my_slot[ks * kDecThreads] : 0u;
+            if (k > 0) my_slot[ks * kDecThreads] = 0u;
+            P -= (int)(ev >> 11);
+            R4 -= (int)(ev & 0x7FFu);
+            const float m2P = __fmul_rn((float)P, nsc);
+            const float R = __fmul_rn((float)R4, 0.25f);
+            const uint32_t lb = lrow[k];
+            const uint32_t lo = lb & 0x7Fu, hi = lo + (lb >> 7);
+            const float glo = cand_err_m2p(s_tab[lo], m2P, R);
+            const float ghi = cand_err_m2p(s_tab[hi], m2P, R);
+            const bool tlo = glo < best_g;
+            best_g = tlo ? glo : best_g;
+            best_i = tlo ? 2 * k : best_i;
+            const bool thi = ghi < best_g;
+            best_g = thi ? ghi : best_g;
+            best_i = thi ? 2 * k + 1 : best_i;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (path == 2) best_i = search_plain(a0, a1, alpha, ev0, d0, s_tab, m_tab, lo_tab);
+    __syncwarp();
+    const int bk = best_i >> 1;
+    const uint32_t lb = lo_tab[d0 * kDecK + bk];
+    const uint32_t best_d = path == 0 ? d0 : ((best_i & 1) ? (lb & 0x7Fu) + (lb >> 7) : (lb & 0x7Fu));
+    const float sq = path == 0 ? 0.0f : __fmul_rn(alpha, __fmul_rn(ev0, m_tab[bk]));
+    uint32_t c0, c1;
+    quant16<false>(blk, sq, sq > 0.0f ? __frcp_rn(sq) : 0.0f, c0, c1, P_unused, R_unused);  // zero scale: signs only
+    if (live) {
+      codes32[2 * b] = c0;
+      codes32[2 * b + 1] = c1;
+      scales[b] = (uint8_t)best_d;
+    }
+    a0 = n0;
+    a1 = n1;
+  }
+}
+
+cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
+                             uint8_t *codes, int sms, cudaStream_t st) {
+  const int64_t need = (B + kDecThreads - 1) / kDecThreads;
+  const int grid = (int)(need < sms ? (need < 1 ? 1 : need) : sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_decoupled, static_cast<const uint4 *>(W), B, alpha_hist, t, scales,
+                            reinterpret_cast<uint32_t *>(codes));
+}
+
+cudaError_t prepare_decoupled_kernel() {
+  return cudaFuncSetAttribute(k_decoupled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecSmem);
+}
+
+}  // namespace nvfp4

@@ -8,7 +8,7 @@
 namespace nvfp4 {
 
 enum { kModeMax = 0, kModeFourOverSix = 1, kModeCjso = 2, kModeCjsoDecoupled = 3 };
-enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDecoupled, kKernDequant, kKernGroupAmax,
+enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDequant, kKernGroupAmax,
        kKernGroupQuantMax, kKernGroupQuantFos, kKernAmaxLdg, kKernCount };
 
 // A group of tensors for the grouped max-rule / FourOverSix kernels, passed by
@@ -41,7 +41,7 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
                        uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                        int grid, cudaStream_t st);
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,
-                             int grid, int split, cudaStream_t st);
+                             int sms, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out, int grid,
                     cudaStream_t st);
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);
@@ -63,6 +63,11 @@ cudaError_t launch_gemm_tc_reduce(const float *ws, int64_t rows, int64_t cols, i
                                   int grid, cudaStream_t st);
 cudaError_t prepare_gemm_tc_kernels();
 cudaError_t prepare_decoupled_kernel();
+cudaError_t prepare_quant_kernels();
 int max_active_ctas(int which);
+int64_t ffma_probe_fmas_per_thread(int packed, int64_t rounds);
+cudaError_t launch_ffma_probe(int packed, int64_t rounds, int grid, float *sink, cudaStream_t st);
+int ffma_probe_threads();
+int ffma_probe_occupancy(int packed);
 
 }  // namespace nvfp4

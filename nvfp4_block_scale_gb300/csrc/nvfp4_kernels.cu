@@ -14,7 +14,6 @@
 //   [SOAR-D]   same page: closed form for a block scale Delta_i*.
 //   [SOAR-SCHED] same page: CJSO schedule (max-rule start, re-quantize after
 //              every update).
-//   [SOAR-DEC] same page: decoupled quantization/dequantization scale search.
 //   [FOS-02]   "SOAR 周冠军笔记 07 | 香草小张：NVFP4 量化改进与推测解码实践",
 //              section 02 (FourOverSix).
 #include <cuda_runtime.h>
@@ -441,118 +440,6 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
 }
 
 // ---------------------------------------------------------------------------
-// a6: decoupled search
-// ---------------------------------------------------------------------------
-//
-// Every candidate constant depends only on (Delta^d0 code, k): the quotient
-// scale sq = fl(alpha * fl(Delta^d0 * m_k)), its reciprocal, and the dequant
-// scales fl(alpha * Delta^d) of the two E4M3 values bracketing Delta^q.  Each
-// CTA tabulates them for all 128 codes x 101 multipliers in shared memory
-// (206,848 bytes), so the search over a block reads one float4 per candidate.
-// One block per thread, held in registers.  [SOAR-DEC]
-constexpr int kDecThreads = 1024;
-constexpr int kDecK = 101;
-constexpr size_t kDecTableBytes = (size_t)128 * kDecK * sizeof(float4);
-
-__device__ __forceinline__ void bracket_e4m3(float dq, const float *ev_tab, uint32_t &lo, uint32_t &hi) {
-  const uint32_t n = e4m3_code(dq);  // the two E4M3 values around dq (448 above 448)
-  const float vn = ev_tab[n];
-  lo = vn > dq ? n - 1u : n;
-  hi = vn < dq ? min(n + 1u, 0x7Eu) : n;
-}
-
-// SPLIT consecutive lanes share one block: lane `sub` of the group evaluates
-// k = sub, sub + SPLIT, ... in ascending order, keeping its first strict
-// minimum; the group then takes the least (g, 2k + h) over its lanes, which
-// is the first strict minimum over all 202 candidates in (k, lower-before-
-// upper) order.  SPLIT > 1 serves tensors with fewer blocks than the GPU has
-// threads.  Every lane of a warp runs the same number of iterations (lanes
-// past the last block idle inside), so the shuffles see the whole warp.
-template <int SPLIT>
-__global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
-                                                              const float *__restrict__ alpha_hist, int t,
-                                                              uint8_t *__restrict__ scales,
-                                                              uint32_t *__restrict__ codes32) {
-  extern __shared__ float4 tab[];  // [code][k] = {sq, rq, sd_lo, sd_hi}
-  __shared__ float ev_tab[128], m_tab[kDecK];
-  const int sub = threadIdx.x % SPLIT;
-  const int64_t per_cta = kDecThreads / SPLIT;  // blocks per CTA and iteration
-  const int64_t stride = (int64_t)gridDim.x * per_cta;
-  const int64_t warp_first = ((int64_t)blockIdx.x * kDecThreads + (threadIdx.x & ~31)) / SPLIT;
-  int64_t b = ((int64_t)blockIdx.x * kDecThreads + threadIdx.x) / SPLIT;
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
-  if (threadIdx.x < 128) ev_tab[threadIdx.x] = e4m3_value(threadIdx.x);
-  if (threadIdx.x < kDecK)  // m_k = fl32((50 + k) / 100)
-    m_tab[threadIdx.x] = __double2float_rn(__ddiv_rn((double)(50 + threadIdx.x), 100.0));
-  pdl_launch_dependents();
-  pdl_wait();
-  const float alpha = alpha_hist[t];
-  __syncthreads();
-  for (int e = threadIdx.x; e < 128 * kDecK; e += kDecThreads) {
-    const int c = e / kDecK, k = e - c * kDecK;
-    const float dq = __fmul_rn(ev_tab[c], m_tab[k]);
-    const float sq = __fmul_rn(alpha, dq);
-    uint32_t lo, hi;
-    bracket_e4m3(dq, ev_tab, lo, hi);
-    tab[e] = make_float4(sq, sq > 0.0f ? __frcp_rn(sq) : 0.0f, __fmul_rn(alpha, ev_tab[lo]),
-                         __fmul_rn(alpha, ev_tab[hi]));
-  }
-  __syncthreads();
-
-  for (int64_t wf = warp_first; wf < B; wf += stride, b += stride) {  // wf: the warp's first block
-    const bool live = b < B;
-    const int64_t nb = b + stride;
-    const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
-    Block16 blk;
-    const uint32_t am = unpack16(a0, a1, blk);
-    const uint32_t d0 = live ? scales[b] : 0u;
-    const bool search = live && __fmul_rn(alpha, ev_tab[d0]) != 0.0f;
-    float best_g = __int_as_float(0x7F800000);  // +inf
-    int best_i = 2 * kDecK;                      // candidate index 2k + h
-    if (search) {
-      BlockH16 bh;
-      make_h16(blk, am, bh);
-      const float4 *row = tab + d0 * kDecK;
-      for (int k = sub; k < kDecK; k += SPLIT) {
-        const float4 c = row[k];
-        float m2P, R;
-        block_sums_h(blk, bh, c.x, c.y, m2P, R);
-        const float glo = cand_err_m2p(c.z, m2P, R);
-        const float ghi = cand_err_m2p(c.w, m2P, R);
-        if (glo < best_g) { best_g = glo; best_i = 2 * k; }
-        if (ghi < best_g) { best_g = ghi; best_i = 2 * k + 1; }
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < SPLIT; o <<= 1) {  // least (g, index) over the group's lanes
-      const float g2 = __shfl_xor_sync(0xFFFFFFFFu, best_g, o);
-      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, best_i, o);
-      if (g2 < best_g || (g2 == best_g && i2 < best_i)) { best_g = g2; best_i = i2; }
-    }
-    if (live && sub == 0) {
-      uint32_t best_d = d0, c0, c1;
-      float P, R;
-      if (search) {
-        const int best_k = best_i >> 1;
-        const float4 c = tab[d0 * kDecK + best_k];
-        quant16<false>(blk, c.x, c.y, c0, c1, P, R);
-        uint32_t lo, hi;
-        bracket_e4m3(__fmul_rn(ev_tab[d0], m_tab[best_k]), ev_tab, lo, hi);
-        best_d = (best_i & 1) ? hi : lo;
-      } else {
-        quant16<false>(blk, 0.0f, 0.0f, c0, c1, P, R);  // zero scale: sign-only codes
-      }
-      codes32[2 * b] = c0;
-      codes32[2 * b + 1] = c1;
-      scales[b] = (uint8_t)best_d;
-    }
-    a0 = n0;
-    a1 = n1;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // a1-a4, a7 over a group of tensors (max rule and FourOverSix)
 // ---------------------------------------------------------------------------
 //
@@ -883,23 +770,6 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
                             alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha, descending);
 }
 
-cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
-                             uint8_t *codes, int grid, int split, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = make_cfg(grid, st);
-  cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = kDecTableBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const uint4 *w = static_cast<const uint4 *>(W);
-  uint32_t *c = reinterpret_cast<uint32_t *>(codes);
-  if (split == 4) return cudaLaunchKernelEx(&cfg, k_decoupled<4>, w, B, alpha_hist, t, scales, c);
-  if (split == 2) return cudaLaunchKernelEx(&cfg, k_decoupled<2>, w, B, alpha_hist, t, scales, c);
-  return cudaLaunchKernelEx(&cfg, k_decoupled<1>, w, B, alpha_hist, t, scales, c);
-}
-
 cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   cudaLaunchAttribute attr[1];
@@ -921,15 +791,8 @@ cudaError_t launch_group_quant(int mode, const GroupArgs &g, const uint32_t *ama
   return cudaLaunchKernelEx(&cfg, k_group_quant<kModeMax>, g, amax);
 }
 
-cudaError_t prepare_decoupled_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(k_decoupled<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_decoupled<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_decoupled<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecTableBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_amax_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAmaxBulkSmem);
-  return e;
+cudaError_t prepare_quant_kernels() {
+  return cudaFuncSetAttribute(k_amax_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAmaxBulkSmem);
 }
 
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out,
@@ -966,9 +829,6 @@ int max_active_ctas(int which) {
     case kKernQuantMax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeMax>, kThreads, 0); break;
     case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
     case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
-    case kKernDecoupled:
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decoupled<1>, kDecThreads, kDecTableBytes);
-      break;
     case kKernAmaxLdg: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
     case kKernGroupAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_amax, kThreads, 0); break;
     case kKernGroupQuantMax:

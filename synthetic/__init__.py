@@ -17,7 +17,8 @@ available here); see the workload table below.
   mlp_up      4096 x 14336    410 seeded rows (10 %) N(0, 0.05), rest N(0, 0.015)
   llama3_8b   32 layers x {q 4096^2, k/v 1024x4096, o 4096^2, gate/up 14336x4096,
               down 4096x14336}; Student-t df=5 scaled to std 0.02, one seed per tensor
-  mlp_70b     8192 x 28672    N(0, 0.01); 117,441 seeded entries (0.05 %) set to
+  mlp_70b     8192 x 28672    N(0, 0.01) (row chunks from child streams of the
+                              seed); 117,441 seeded entries (0.05 %) set to
                               +-U(0.3, 1.0) with random sign
 """
 from __future__ import annotations
@@ -102,10 +103,33 @@ def llama3_8b_tensor(index: int, seed_base: int = 1000, layers: int = 32) -> np.
     return student_t(rows, cols, 5.0, 0.02, seed_base + index)
 
 
+def _parallel_normal(rows: int, cols: int, std: float, seed: int, chunk_rows: int = 128) -> np.ndarray:
+    """N(0, std) float32 [rows, cols], drawn in chunks of `chunk_rows` rows on
+    host threads; chunk c uses its own PCG64 stream, the c-th child of
+    SeedSequence(seed), so the result does not depend on the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    a = np.empty((rows, cols), np.float32)
+    nch = (rows + chunk_rows - 1) // chunk_rows
+    seqs = np.random.SeedSequence(seed).spawn(nch)
+
+    def fill(c):
+        part = a[c * chunk_rows:(c + 1) * chunk_rows]
+        np.random.Generator(np.random.PCG64(seqs[c])).standard_normal(part.shape, dtype=np.float32, out=part)
+        part *= np.float32(std)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(nch)))
+    return a
+
+
 def mlp_70b(seed: int = 4, rows: int = 8192, cols: int = 28672) -> np.ndarray:
-    """N(0, 0.01) with 0.05 % of entries set to +-U(0.3, 1.0)."""
+    """N(0, 0.01) with 0.05 % of entries set to +-U(0.3, 1.0).  The Gaussian
+    part is drawn in row chunks from child streams of SeedSequence(seed)
+    (host threads); the outlier positions, magnitudes and signs come from
+    default_rng(seed)."""
     rng = np.random.default_rng(seed)
-    a = rng.standard_normal((rows, cols), dtype=np.float32) * np.float32(0.01)
+    a = _parallel_normal(rows, cols, 0.01, seed)
     n = rows * cols
     k = int(round(0.0005 * n))
     pos = rng.choice(n, size=k, replace=False)

@@ -1,8 +1,9 @@
 """Parity at the benchmark workloads' full sizes, in the same launch
 configuration the benchmark times.  The oracle computes alpha and every CJSO
-iteration on the whole tensor; where the per-block final pass is too slow on
-the CPU (decoupled search, the 8192x28672 tensor) it is computed for a seeded
-sample of blocks, including the first and last block."""
+iteration on the whole tensor and, except for the decoupled search, every
+block; the decoupled search's final pass (about 100x the oracle's cost of the
+other rules) is compared on whole row slabs, or on a seeded sample of blocks
+of the stack's tensors."""
 import os
 
 import numpy as np
@@ -71,21 +72,50 @@ def test_mlp_up_full(mlp_up, mode, iters):
     """4096x14336 row mixture: every block compared."""
     gc, gs, ga = check_full(mlp_up, mode, iters)
     if mode == oracle.MAX:
-        rows = slice(0, 64)
-        od = oracle.dequantize(gc[rows], gs[rows], ga, 64, mlp_up.shape[1])
-        assert np.array_equal(gpu_dequantize(gc, gs, ga, *mlp_up.shape)[rows], od)
+        od = oracle.dequantize(gc, gs, ga, *mlp_up.shape)
+        assert np.array_equal(gpu_dequantize(gc, gs, ga, *mlp_up.shape), od)
 
 
-def test_mlp_up_decoupled_sampled(mlp_up):
+def test_mlp_up_decoupled_row_slab(mlp_up):
+    """Decoupled CJSO(5) on the 4096x14336 tensor: rows 0..511 in full (the
+    10 % of hot rows are spread over them), plus a seeded sample elsewhere."""
+    check_rows(mlp_up, oracle.CJSO_DECOUPLED, 5, np.arange(512))
     check_sampled(mlp_up, oracle.CJSO_DECOUPLED, 5)
 
 
-@pytest.mark.parametrize("mode,iters", [(oracle.MAX, 0), (oracle.FOUR_OVER_SIX, 0), (oracle.CJSO, 5),
-                                        (oracle.CJSO_DECOUPLED, 5)])
-def test_mlp_70b_sampled(mode, iters):
-    """8192x28672 N(0, 0.01) with +-U(0.3, 1) spikes (larger than L2)."""
-    w = synthetic.mlp_70b()
-    check_sampled(w, mode, iters, nsample=20000 if mode != oracle.CJSO_DECOUPLED else 4000)
+def check_rows(w, mode, iters, rows):
+    """Every block of the listed rows, against the oracle's final pass on them
+    (alpha and the CJSO iterations over the whole tensor)."""
+    gc, gs, ga = gpu_quantize(w, mode, iters)
+    kb = w.shape[1] // 16
+    blocks = (np.asarray(rows)[:, None] * kb + np.arange(kb)[None, :]).reshape(-1).astype(np.int64)
+    oc, os_, oa = oracle.quantize_sampled(w, mode, iters, blocks, threads=THREADS)
+    assert ga == oa
+    bad = block_mismatch(gc.reshape(-1, 8)[blocks], gs.reshape(-1)[blocks], oc, os_)
+    assert bad.sum() <= int(1e-6 * (w.size // 16)), (bad.sum(), len(blocks))
+    return gc, gs, ga
+
+
+@pytest.fixture(scope="module")
+def mlp_70b():
+    return synthetic.mlp_70b()
+
+
+@pytest.mark.parametrize("mode,iters", [(oracle.MAX, 0), (oracle.FOUR_OVER_SIX, 0), (oracle.CJSO, 5)])
+def test_mlp_70b_full(mlp_70b, mode, iters):
+    """8192x28672 N(0, 0.01) with +-U(0.3, 1) spikes (larger than L2): every
+    block compared; the max-rule output dequantized in full."""
+    gc, gs, ga = check_full(mlp_70b, mode, iters)
+    if mode == oracle.MAX:
+        od = oracle.dequantize(gc, gs, ga, *mlp_70b.shape)
+        assert np.array_equal(gpu_dequantize(gc, gs, ga, *mlp_70b.shape), od)
+
+
+def test_mlp_70b_decoupled_row_slabs(mlp_70b):
+    """Decoupled CJSO(5) on the 8192x28672 tensor: 512 whole rows (the first
+    and last 256), every block of them."""
+    rows = np.r_[0:256, mlp_70b.shape[0] - 256:mlp_70b.shape[0]]
+    check_rows(mlp_70b, oracle.CJSO_DECOUPLED, 5, rows)
 
 
 @pytest.mark.parametrize("index", [0, 1, 4, 6, 223])
