@@ -70,19 +70,25 @@ constexpr float kAmbig = 0x1p-12f;
 // the per-CTA tables.
 constexpr size_t kOffMask = (size_t)kSlotK * kDecThreads * 4;
 constexpr size_t kOffLohi = kOffMask + (size_t)4 * kDecThreads * 4;
-constexpr size_t kOffS = kOffLohi + 128 * 4 * 4;
-constexpr size_t kOffR = kOffS + 128 * 4;
+constexpr size_t kOffS2 = kOffLohi + 128 * 4 * 4;
+constexpr size_t kOffR = kOffS2 + 128 * 8;
 constexpr size_t kOffEv = kOffR + 128 * 4;
 constexpr size_t kOffM = kOffEv + 128 * 4;
-constexpr size_t kOffLo = kOffM + 112 * 4;
+constexpr size_t kOffH = kOffM + 104 * 4;
+constexpr size_t kOffStep = kOffH + 8 * 16;
+constexpr size_t kOffLo = kOffStep + 8 * 8;
 constexpr size_t kDecSmem = kOffLo + 128 * kDecK;
 static_assert(kDecSmem <= 232448, "dynamic shared memory of one CTA");
 
-// fl(100 / b) for the E2M1 decision points b = 0.25, 0.75, 1.25, 1.75, 2.5,
-// 3.5, 5 (b_i lies between magnitude codes i and i + 1).
+// fl(100 / b_i) for the E2M1 decision points b_i = 0.25, 0.75, 1.25, 1.75,
+// 2.5, 3.5, 5 (b_i lies between magnitude codes i and i + 1), and per
+// crossing of b_i: 2(q_{i+1} - q_i) = 1,1,1,1,2,2,4 (as a shift) and
+// 4(q_{i+1}^2 - q_i^2) = 1,3,5,7,20,28,80.
 __constant__ float kHundredOverB[7] = {(float)(100.0 / 0.25), (float)(100.0 / 0.75), (float)(100.0 / 1.25),
                                        (float)(100.0 / 1.75), (float)(100.0 / 2.5),  (float)(100.0 / 3.5),
                                        (float)(100.0 / 5.0)};
+__constant__ uint8_t kStepShift[7] = {0, 0, 0, 0, 1, 1, 2};
+__constant__ uint8_t kStepR4[7] = {1, 3, 5, 7, 20, 28, 80};
 
 // Byte lookups (prmt on two words holding an 8-byte table).
 __device__ __forceinline__ uint32_t lut8(uint32_t lo4, uint32_t hi4, uint32_t idx) {
@@ -91,10 +97,6 @@ __device__ __forceinline__ uint32_t lut8(uint32_t lo4, uint32_t hi4, uint32_t id
 // 2q and 4q^2 of a magnitude code: {0,1,2,3,4,6,8,12}, {0,1,4,9,16,36,64,144}
 __device__ __forceinline__ uint32_t two_q(uint32_t c) { return lut8(0x03020100u, 0x0C080604u, c); }
 __device__ __forceinline__ uint32_t four_q2(uint32_t c) { return lut8(0x09040100u, 0x90402410u, c); }
-// Crossing decision point i (code i+1 -> i): 2(q_{i+1} - q_i) = 1,1,1,1,2,2,4 as
-// a shift, and 4(q_{i+1}^2 - q_i^2) = 1,3,5,7,20,28,80.
-__device__ __forceinline__ uint32_t step_shift(uint32_t i) { return lut8(0x00000000u, 0x00020101u, i); }
-__device__ __forceinline__ uint32_t step_r4(uint32_t i) { return lut8(0x07050301u, 0x00501C14u, i); }
 
 // E4M3 codes bracketing dq >= 0: lo = largest with value <= dq, hi = smallest
 // with value >= dq (448 above 448), packed as lo | (hi != lo) << 7.
@@ -106,18 +108,13 @@ __device__ __forceinline__ uint32_t bracket_byte(float dq, const float *ev_tab) 
   return lo | ((hi != lo ? 1u : 0u) << 7);
 }
 
-__device__ __forceinline__ float elem(const Block16 &blk, int j) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(blk.x[j >> 1]));
-  return (j & 1) ? hi : lo;
-}
-
 // The plain search for blocks outside the exact-integer range: every
 // candidate's P, R from its own quotients (the block's scaled f16 image for P).
-__device__ __noinline__ int search_plain(uint4 a0, uint4 a1, float alpha, float ev0, uint32_t d0,
-                                         const float *s_tab, const float *m_tab, const uint8_t *lo_tab) {
+__device__ __noinline__ int search_plain(const uint4 *__restrict__ W, int64_t b, float alpha, float ev0,
+                                         uint32_t d0, const float2 *s2_tab, const float *m_tab,
+                                         const uint8_t *lo_tab) {
   Block16 blk;
-  const uint32_t am = unpack16(a0, a1, blk);
+  const uint32_t am = unpack16(__ldg(W + 2 * b), __ldg(W + 2 * b + 1), blk);
   BlockH16 bh;
   make_h16(blk, am, bh);
   float best_g = __int_as_float(0x7F800000);
@@ -128,13 +125,28 @@ __device__ __noinline__ int search_plain(uint4 a0, uint4 a1, float alpha, float 
     float m2P, R;
     block_sums_h(blk, bh, sq, r, m2P, R);
     const uint32_t lb = lo_tab[d0 * kDecK + k];
-    const uint32_t lo = lb & 0x7Fu, hi = lo + (lb >> 7);
-    const float glo = cand_err_m2p(s_tab[lo], m2P, R);
-    const float ghi = cand_err_m2p(s_tab[hi], m2P, R);
+    const float2 sp = s2_tab[lb & 0x7Fu];
+    const float glo = cand_err_m2p(sp.x, m2P, R);
+    const float ghi = cand_err_m2p((lb >> 7) ? sp.y : sp.x, m2P, R);
     if (glo < best_g) { best_g = glo; best_i = 2 * k; }
     if (ghi < best_g) { best_g = ghi; best_i = 2 * k + 1; }
   }
   return best_i;
+}
+
+// Signed E2M1 codes of 8 elements with dequant scale s (reciprocal r), one
+// word (element 2k in the low nibble of byte k); r = 0 gives sign-only codes.
+__device__ __forceinline__ uint32_t quant8(const f32x2 (&x)[4], float s, float r) {
+  const f32x2 s2 = pack2(s, s), nr2 = pack2(-r, -r);
+  const uint32_t c = encode8(negdiv2_by_scale(x[0], s2, nr2), negdiv2_by_scale(x[1], s2, nr2),
+                             negdiv2_by_scale(x[2], s2, nr2), negdiv2_by_scale(x[3], s2, nr2));
+  return c ^ 0x88888888u;
+}
+
+__device__ __forceinline__ float elem(const Block16 &blk, int j) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(blk.x[j >> 1]));
+  return (j & 1) ? hi : lo;
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
@@ -145,12 +157,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   uint32_t *slot = reinterpret_cast<uint32_t *>(dsm);            // [k - 1][thread]
   uint32_t *mask = reinterpret_cast<uint32_t *>(dsm + kOffMask);  // [word][thread]
   uint32_t *lohi = reinterpret_cast<uint32_t *>(dsm + kOffLohi);  // [Delta^d0 code][word]
-  float *s_tab = reinterpret_cast<float *>(dsm + kOffS);          // fl(alpha * value)
-  float *r_tab = reinterpret_cast<float *>(dsm + kOffR);          // its IEEE reciprocal
+  float2 *s2_tab = reinterpret_cast<float2 *>(dsm + kOffS2);      // fl(alpha * value) of codes c, c + 1
+  float *r_tab = reinterpret_cast<float *>(dsm + kOffR);          // IEEE reciprocal of fl(alpha * value)
   float *ev_tab = reinterpret_cast<float *>(dsm + kOffEv);        // E4M3 values
-  float *m_tab = reinterpret_cast<float *>(dsm + kOffM);          // m_k (101), then fl(100 / b_i) (7)
+  float *m_tab = reinterpret_cast<float *>(dsm + kOffM);          // m_k
+  float4 *h_rows = reinterpret_cast<float4 *>(dsm + kOffH);       // [code c]: fl(100/b) of c-1 .. c-4
+  uint2 *step_rows = reinterpret_cast<uint2 *>(dsm + kOffStep);   // [code c]: shifts, R4 steps (bytes)
   uint8_t *lo_tab = dsm + kOffLo;                                 // [Delta^d0 code][k] bracket byte
-  float *h_tab = m_tab + kDecK;
   const int tid = threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kDecThreads;
   const int64_t warp_first = (int64_t)blockIdx.x * kDecThreads + (tid & ~31);
@@ -159,12 +172,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   uint4 a0 = b < B ? __ldg(W + 2 * b) : z, a1 = b < B ? __ldg(W + 2 * b + 1) : z;
 
   // alpha-independent set-up, overlapping the previous kernel's tail
-  for (int k = 0; k < kSlotK; ++k) slot[k * kDecThreads + tid] = 0u;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) mask[w * kDecThreads + tid] = 0u;
+  for (int e = tid; e < kSlotK * kDecThreads; e += kDecThreads) slot[e] = 0u;
+  for (int e = tid; e < 4 * kDecThreads; e += kDecThreads) mask[e] = 0u;
   if (tid < 128) ev_tab[tid] = e4m3_value(tid);
   if (tid < kDecK) m_tab[tid] = __double2float_rn(__ddiv_rn((double)(50 + tid), 100.0));  // m_k
-  if (tid < 7) h_tab[tid] = kHundredOverB[tid];
+  if (tid < 8) {  // crossing constants of magnitude code c = tid, steps st = 0..3 -> decision point c-1-st
+    float hv[4];
+    uint32_t sh = 0u, r4 = 0u;
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+      const int i = tid - 1 - st;
+      hv[st] = i >= 0 ? kHundredOverB[i] : 0.0f;
+      sh |= (uint32_t)(i >= 0 ? kStepShift[i] : 0) << (8 * st);
+      r4 |= (uint32_t)(i >= 0 ? kStepR4[i] : 0) << (8 * st);
+    }
+    h_rows[tid] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    step_rows[tid] = make_uint2(sh, r4);
+  }
   __syncthreads();
   for (int e = tid; e < 128 * kDecK; e += kDecThreads) {
     const int c = e / kDecK, k = e - c * kDecK;
@@ -193,7 +217,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   const float alpha = alpha_hist[t];
   if (tid < 128) {
     const float s = __fmul_rn(alpha, ev_tab[tid]);
-    s_tab[tid] = s;
+    const float s1 = tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f;
+    s2_tab[tid] = make_float2(s, s1);
     r_tab[tid] = s > 0.0f ? __frcp_rn(s) : 0.0f;
   }
   __syncthreads();
@@ -208,47 +233,51 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
     const uint32_t d0 = live ? scales[b] : 0u;
-    const float s50 = s_tab[d0];
+    const float s50 = s2_tab[d0].x;
     const float r50 = r_tab[d0];
     const float ev0 = ev_tab[d0];
     const int e_a = (int)(am >> 7);  // biased exponent of the block maximum
-    const float sc = __uint_as_float((uint32_t)(268 - min(max(e_a, 15), 254)) << 23);  // 2^E, E = 141 - e_a
+    const int e_c = min(max(e_a, 15), 230);
+    const float sc = __uint_as_float((uint32_t)(268 - e_c) << 23);  // 2^E, E = 141 - e_a
     // 0: zero scale (sign-only codes); 1: event scan; 2: plain loop
-    int path = !(s50 > 0.0f) ? 0 : ((e_a >= 15 && __fmul_rn(s50, sc) >= 1025.0f) ? 1 : 2);
-    float P_unused, R_unused;
+    int path = !(s50 > 0.0f) ? 0 : ((e_a == e_c && __fmul_rn(s50, sc) >= 1025.0f) ? 1 : 2);
     int best_i = 0;
     if (path == 1) {
-      const float nsc = -__uint_as_float((uint32_t)(max(e_a, 15) - 14) << 23);  // -2^-E
+      const float nsc = -__uint_as_float((uint32_t)(e_c - 14) << 23);  // -2^-E
       // exact magnitude codes at k = 0 (sq_0 = s50 / 2, its reciprocal 2 / s50)
-      uint32_t q0, q1;
-      quant16<false>(blk, __fmul_rn(s50, 0.5f), __fmul_rn(r50, 2.0f), q0, q1, P_unused, R_unused);
-      q0 &= 0x77777777u;
-      q1 &= 0x77777777u;
+      const float s0 = __fmul_rn(s50, 0.5f), r0 = __fmul_rn(r50, 2.0f);
+      const uint32_t qw[2] = {quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[0]), s0, r0) & 0x77777777u,
+                              quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[4]), s0, r0) & 0x77777777u};
       int P = 0, R4 = 0;  // P = P_int * 2^(-E-1), R = R4 / 4
       bool amb = false;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float xa = fabsf(elem(blk, j));
-        const uint32_t c = ((j < 8 ? q0 : q1) >> (4 * (j & 7))) & 7u;
+        const uint32_t c = (qw[j >> 3] >> (4 * (j & 7))) & 7u;
         const uint32_t X = __float2uint_rz(__fmul_rn(xa, sc));
         P += (int)(X * two_q(c));
         R4 += (int)four_q2(c);
         const float v = __fmul_rn(xa, r50);
+        const float4 hr = h_rows[c];
+        const uint2 sr = step_rows[c];
+        const float hv[4] = {hr.x, hr.y, hr.z, hr.w};
+        const uint32_t X11 = X << 11;
         bool go = true;
 #pragma unroll
         for (int st = 0; st < 4; ++st) {  // the element's crossings, in k order: decision points c-1, c-2, ...
-          const int i = (int)c - 1 - st;
-          go = go && i >= 0;
-          const int ii = max(i, 0);
-          const float kap = __fmaf_rn(v, h_tab[ii], -50.0f);
-          const float n = rintf(kap);
-          // within kAmbig of an integer n in 1..100 the crossing may be at n or n + 1
-          // (near 0 it is at 1: the code at k = 0 is known)
-          amb = amb || (go && n >= 1.0f && n <= 100.0f && fabsf(__fsub_rn(kap, n)) < kAmbig);
-          const int K = max((int)ceilf(kap), 1);
+          go = go && (int)c > st;
+          const float kap = __fmaf_rn(v, hv[st], -50.0f);
+          // kap rounded to the nearest integer n (|kap| < 2^22), and K = ceil(kap)
+          const float tt = __fadd_rn(kap, 12582912.0f);
+          const int n = __float_as_int(tt) - 0x4B400000;
+          const float frac = __fsub_rn(kap, __fsub_rn(tt, 12582912.0f));
+          // within kAmbig of an integer the crossing may be at n or n + 1
+          amb = amb || (go && fabsf(frac) < kAmbig);
+          const int K = max(n + (frac > 0.0f ? 1 : 0), 1);
           go = go && K <= kSlotK;
           if (go) {
-            atomicAdd(my_slot + (K - 1) * kDecThreads, (X << (11 + step_shift(ii))) + step_r4(ii));
+            atomicAdd(my_slot + (K - 1) * kDecThreads,
+                      (X11 << ((sr.x >> (8 * st)) & 0xFFu)) + ((sr.y >> (8 * st)) & 0xFFu));
             atomicOr(my_mask + (K >> 5) * kDecThreads, 1u << (K & 31));
           }
         }
@@ -268,6 +297,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
       } else {
         // scan the breakpoints in k order
         float best_g = __int_as_float(0x7F800000);
+        const float c23 = __fmul_rn(-8388608.0f, nsc);
         const uint32_t *lm = lohi + d0 * 4;
         const uint8_t *lrow = lo_tab + d0 * kDecK;
 #pragma unroll
@@ -282,12 +312,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
             if (k > 0) my_slot[ks * kDecThreads] = 0u;
             P -= (int)(ev >> 11);
             R4 -= (int)(ev & 0x7FFu);
-            const float m2P = __fmul_rn((float)P, nsc);
-            const float R = __fmul_rn((float)R4, 0.25f);
+            // exact int -> float: (2^23 + v) - 2^23, folded into the scaling
+            const float m2P = __fmaf_rn(__uint_as_float((uint32_t)P | 0x4B000000u), nsc, c23);
+            const float R = __fmaf_rn(__uint_as_float((uint32_t)R4 | 0x4B000000u), 0.25f, -2097152.0f);
             const uint32_t lb = lrow[k];
-            const uint32_t lo = lb & 0x7Fu, hi = lo + (lb >> 7);
-            const float glo = cand_err_m2p(s_tab[lo], m2P, R);
-            const float ghi = cand_err_m2p(s_tab[hi], m2P, R);
+            const float2 sp = s2_tab[lb & 0x7Fu];
+            const float glo = cand_err_m2p(sp.x, m2P, R);
+            const float ghi = cand_err_m2p((lb >> 7) ? sp.y : sp.x, m2P, R);
             const bool tlo = glo < best_g;
             best_g = tlo ? glo : best_g;
             best_i = tlo ? 2 * k : best_i;
@@ -299,14 +330,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
       }
     }
     __syncwarp();
-    if (path == 2) best_i = search_plain(a0, a1, alpha, ev0, d0, s_tab, m_tab, lo_tab);
+    if (path == 2) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
     __syncwarp();
     const int bk = best_i >> 1;
     const uint32_t lb = lo_tab[d0 * kDecK + bk];
-    const uint32_t best_d = path == 0 ? d0 : ((best_i & 1) ? (lb & 0x7Fu) + (lb >> 7) : (lb & 0x7Fu));
+    const uint32_t best_d = path == 0 ? d0 : (lb & 0x7Fu) + ((best_i & 1) ? (lb >> 7) : 0u);
     const float sq = path == 0 ? 0.0f : __fmul_rn(alpha, __fmul_rn(ev0, m_tab[bk]));
-    uint32_t c0, c1;
-    quant16<false>(blk, sq, sq > 0.0f ? __frcp_rn(sq) : 0.0f, c0, c1, P_unused, R_unused);  // zero scale: signs only
+    const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;  // zero scale: signs only
+    const uint32_t c0 = quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[0]), sq, rq);
+    const uint32_t c1 = quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[4]), sq, rq);
     if (live) {
       codes32[2 * b] = c0;
       codes32[2 * b + 1] = c1;
