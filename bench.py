@@ -54,7 +54,8 @@ sys.path.insert(0, ROOT)
 METRIC = "NVFP4 quantize GB/s (bf16 in) per mode; % of HBM or FP32 roofline, 1 GB300"
 HEADLINE = "mlp_70b"
 MODE_IDS = {"max": 0, "four_over_six": 1, "cjso": 2, "cjso_decoupled": 3, "dequant": 4, "gemv": 5, "swizzle": 6,
-            "gemm": 7}
+            "gemm": 7, "max_noalloc": 8, "four_over_six_noalloc": 9}
+QUANTIZERS = (0, 1, 2, 3, 8, 9)  # modes that quantize W (8, 9: the allocation-free entry point, rule 0 or 1)
 CONSUMERS = ("dequant", "gemv", "swizzle", "gemm")  # modes that read a quantized tensor instead of producing one
 HOT_PATH = ("max", "four_over_six", "cjso", "cjso_decoupled", "dequant")
 
@@ -86,14 +87,14 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 def kernels_per_call(mode: int, iters: int) -> int:
     """Kernels one call launches: amax + quantize; amax + init sweep + one
     sweep per iteration (+ the search); one kernel for the consumers."""
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1, 7: 2}[mode]
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1, 7: 2, 8: 2, 9: 2}[mode]
 
 
 def algorithmic(mode: int, iters: int, n: int, l2_bytes: int, batch: int = 1, hbm_gbs: float = 6660.0,
                 tc_tflops: float = 1884.6):
     """(bound, unit, algorithmic work of one call, rule) for a mode."""
     fits = 2 * n <= l2_bytes // 2
-    if mode in (0, 1):
+    if mode in (0, 1, 8, 9):
         b = ONE_PASS if fits else TWO_PASS
         return "hbm", "GB/s", b * n, f"{b} B/elem ({'W <= L2/2: one HBM read' if fits else 'W read twice'})"
     if mode == 4:  # dequantize: codes + scales in, bf16 out
@@ -346,7 +347,7 @@ def run_ours(args, modes):
     # written back to HBM as a real sequence of tensors would be
     outs = {m: [(torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
                  torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev),
-                 torch.empty(1, dtype=torch.float32, device=dev)) for _ in range(ncopy)] for m in mids if m < 4}
+                 torch.empty(1, dtype=torch.float32, device=dev)) for _ in range(ncopy)] for m in mids if m in QUANTIZERS}
 
     if any(m >= 4 for m in mids):  # consumer inputs: this tensor quantized (max rule) once per rotation slot
         dq_in = []
@@ -362,7 +363,11 @@ def run_ours(args, modes):
         return next(k for k in range(ncopy) if Wd[k] is w)
 
     def call(mode, w, s):
-        if mode == 6:  # the slot's scales into the tensor-core layout
+        if mode in (8, 9):  # the allocation-free entry point (max rule / FourOverSix)
+            c, sc, a = outs[mode][slot_of(w)]
+            st = nv.nvfp4_quantize_noalloc(w.data_ptr(), rows, cols, mode - 8, c.data_ptr(), sc.data_ptr(),
+                                           a.data_ptr(), s.cuda_stream)
+        elif mode == 6:  # the slot's scales into the tensor-core layout
             st = nv.nvfp4_swizzle_scales(dq_in[slot_of(w)][1].data_ptr(), rows, cols, gz.data_ptr(), s.cuda_stream)
         elif mode == 7:  # tensor-core product of `batch` vectors with the slot's quantized tensor
             c, sc, a = dq_in[slot_of(w)]
@@ -542,7 +547,7 @@ def run_ours(args, modes):
               "kernels_event_bracketed": {kn: {"launches": c, "avg_us": t / c * 1e3} for kn, (c, t) in rep.items()}}
         if bound == "alu":
             pm["roofline"]["frac_of_derived_peak"] = achieved / fp32["derived_at_sampled_clock"]
-        if m < 4:  # reconstruction error of this mode's output, in double
+        if m in QUANTIZERS:  # reconstruction error of this mode's output, in double
             c, sc, a = outs[m][0]
             pm["mse"] = mse_on_device(Wd[0], c, sc, a)
         per_mode[name] = pm
@@ -581,7 +586,7 @@ def run_ours(args, modes):
     # pipelined over two buffer slots and three streams, so the copies of one
     # step overlap the kernels of its neighbours.
     W_pin = W_host.pin_memory()
-    qmids = [m for m in mids if m < 4]
+    qmids = [m for m in mids if m in QUANTIZERS]
     with_dq = 4 in mids
     slots = []
     for _ in range(2):
@@ -596,8 +601,12 @@ def run_ours(args, modes):
 
     def qcall(mode, w, o, st):
         c, sc, a = o
-        r = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
-                              a.data_ptr(), st.cuda_stream)
+        if mode in (8, 9):
+            r = nv.nvfp4_quantize_noalloc(w.data_ptr(), rows, cols, mode - 8, c.data_ptr(), sc.data_ptr(),
+                                          a.data_ptr(), st.cuda_stream)
+        else:
+            r = nv.nvfp4_quantize(w.data_ptr(), rows, cols, mode, args.iters, c.data_ptr(), sc.data_ptr(),
+                                  a.data_ptr(), st.cuda_stream)
         if r != 0:
             raise RuntimeError(f"nvfp4_quantize: {nv.nvfp4_status_string(r)}")
 

@@ -114,12 +114,15 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
  *           not overlap each other or any W.
  *   count   >= 0 (0: nothing is enqueued).  Longer lists are processed in
  *           consecutive slices of NVFP4_GROUP_MAX tensors.  A list holding at
- *           least 16 x L2 bytes of bf16 is cut into 8 parts of about equal
- *           size that alternate between `stream` and a second stream owned
- *           by the library (forked from `stream` and joined back into it by
- *           events, so the call can be captured in a CUDA graph), letting one
- *           part's max|W| pass overlap another part's quantize pass; calls
- *           from several host threads take turns on that second stream.
+ *           least 4 x L2 bytes of bf16 is cut into parts of about 3 x L2
+ *           that alternate between `stream` and a second stream owned by the
+ *           library (forked from `stream` and joined back into it by events,
+ *           so the call can be captured in a CUDA graph), letting one part's
+ *           max|W| pass overlap another part's quantize pass.  The library
+ *           keeps a small pool of such second streams per device: a call
+ *           takes one that no other call holds and that is not part of an
+ *           unfinished stream capture, so concurrent calls from several host
+ *           threads, captured or not, never share one.
  *   mode, iters, stream  as for nvfp4_quantize.  Modes 2 and 3 run the
  *           nvfp4_quantize launch sequence tensor by tensor (their search and
  *           sweeps, not launches, dominate), tensors alternating between
@@ -253,7 +256,11 @@ int nvfp4_encode_e4m3(const float *v, int64_t n, uint8_t *out, cudaStream_t stre
  *     results: serialize them.
  *   - The first call on a device performs a one-time set-up with that device
  *     current (it looks up the array's device address); make that first call
- *     before any stream capture.
+ *     before any stream capture.  Under CUDA's lazy module loading (the
+ *     default) that look-up can be what loads the library's device code onto
+ *     the GPU, which allocates device memory (the array among it) and can
+ *     then fail with NVFP4_ERR_OUT_OF_MEMORY: make the first call at start-up,
+ *     before the caller reserves its memory.
  * Arguments, layouts, alignment and the other statuses are those of
  * nvfp4_quantize (without `iters`).
  */
@@ -298,6 +305,27 @@ int nvfp4_profiler_get(int index, char *name, int name_len, int64_t *launches, d
  */
 int nvfp4_ffma_probe(int packed, int64_t rounds, float *sink, int64_t sink_floats, int64_t *fmas,
                      cudaStream_t stream);
+
+/*
+ * Test hooks.  No counterpart on the method's pages: they let tests drive the
+ * library's failure paths without faulting anything.  Process-wide settings
+ * that every later call sees; meant for test programs, not for use while other
+ * calls are being made.
+ *   nvfp4_test_fail_allocations(count): the next `count` scratch allocations
+ *     fail as if the device were out of memory; a call that meets one returns
+ *     NVFP4_ERR_OUT_OF_MEMORY with nothing enqueued.  count >= 0 (0 clears).
+ *   nvfp4_test_first_wait_tries(tries): tries >= 0 makes the first bounded
+ *     wait of every CTA of later launches give up after that many polls (0:
+ *     at once): in nvfp4_quantize's bulk-copy max|W| pass (tensors larger
+ *     than half of L2) the wait for the CTA's first copy, so alpha comes out
+ *     NaN; in nvfp4_gemm the first wait of the MMA-issuing thread, so the
+ *     outputs come out NaN.  Every copy and MMA already issued still
+ *     completes before the CTA exits (those waits keep their normal limits).
+ *     tries < 0 restores the normal limits.
+ * Both return an nvfp4_status.
+ */
+int nvfp4_test_fail_allocations(int count);
+int nvfp4_test_first_wait_tries(int64_t tries);
 
 /* Human-readable text for a status code (static storage, never NULL). */
 const char *nvfp4_status_string(int status);

@@ -79,6 +79,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_profiler_get.restype = ci
     L.nvfp4_ffma_probe.argtypes = [ci, i64, vp, i64, ctypes.POINTER(ctypes.c_int64), vp]
     L.nvfp4_ffma_probe.restype = ci
+    L.nvfp4_test_fail_allocations.argtypes = [ci]
+    L.nvfp4_test_fail_allocations.restype = ci
+    L.nvfp4_test_first_wait_tries.argtypes = [i64]
+    L.nvfp4_test_first_wait_tries.restype = ci
     L.nvfp4_status_string.argtypes = [ci]
     L.nvfp4_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -137,6 +141,16 @@ def nvfp4_encode_e4m3(v, n, out, stream) -> int:
 def nvfp4_ffma_probe(packed, rounds, sink, sink_floats, fmas, stream) -> int:
     """fp32 FMA throughput probe (instrumentation); `fmas` is a ctypes int64 pointer."""
     return load().nvfp4_ffma_probe(packed, rounds, sink, sink_floats, fmas, stream)
+
+
+def nvfp4_test_fail_allocations(count) -> int:
+    """Test hook: the next `count` scratch allocations fail (out of memory)."""
+    return load().nvfp4_test_fail_allocations(int(count))
+
+
+def nvfp4_test_first_wait_tries(tries) -> int:
+    """Test hook: the first bounded device wait gives up after `tries` polls (< 0: normal)."""
+    return load().nvfp4_test_first_wait_tries(int(tries))
 
 
 def nvfp4_status_string(status: int) -> str:

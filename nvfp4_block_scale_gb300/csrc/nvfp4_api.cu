@@ -14,6 +14,7 @@
 // Grid-wide dependencies are kernel boundaries: no kernel waits on another
 // CTA, so nothing can spin.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -31,6 +32,10 @@ using namespace nvfp4;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxIters = 64;
 constexpr int64_t kMaxElems = int64_t(1) << 40;
+// grouped max rule / FourOverSix: groups of at least kPipeMinL2 x L2 bytes of
+// bf16 run in parts of about kPipePartL2 x L2 on two streams
+constexpr int kPipeMinL2 = 4;
+constexpr int kPipePartL2 = 3;
 
 struct DevInfo {
   bool ready = false;
@@ -39,15 +44,36 @@ struct DevInfo {
   int l2 = 0;  // L2 bytes
   int occ[kKernCount] = {};
   cudaMemPool_t pool = nullptr;
-  // second stream and fork/join events of the pipelined grouped quantization;
-  // `side_mu` keeps one caller at a time on them
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  // second streams (with their fork/join events) of the pipelined grouped
+  // quantization: a caller takes one that no other call holds and that is not
+  // part of an unfinished stream capture (a captured call's second stream
+  // stays in that capture until the caller ends it), creating one if none is
+  // free
+  struct Side {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool busy = false;
+  };
   std::mutex side_mu;
+  std::vector<Side *> sides;
 };
 
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
+
+// test hooks (nvfp4_test_*): allocations left to fail, and the first-wait
+// limit passed to the kernels with bounded waits (< 0: normal)
+std::atomic<int> g_fail_allocs{0};
+std::atomic<long> g_first_wait{-1};
+
+// Scratch from the library's pool on `stream` (or a failure the test hook asked for).
+cudaError_t pool_alloc(void **p, size_t bytes, cudaMemPool_t pool, cudaStream_t stream) {
+  int n = g_fail_allocs.load();
+  while (n > 0 && !g_fail_allocs.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n > 0) return cudaErrorMemoryAllocation;
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
 
 int map_cuda(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4_OK;
@@ -90,9 +116,6 @@ int device_info(DevInfo **out) {
       if (e != cudaSuccess) return map_cuda(e);
       uint64_t keep = UINT64_MAX;
       e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
       if (e != cudaSuccess) return map_cuda(e);
       d.status = NVFP4_OK;
     }
@@ -100,6 +123,43 @@ int device_info(DevInfo **out) {
   }
   *out = &d;
   return d.status;
+}
+
+// A second stream for one grouped call (see DevInfo::Side); nullptr with *err
+// set if none could be made.
+DevInfo::Side *side_acquire(DevInfo &d, cudaError_t *err) {
+  std::lock_guard<std::mutex> lock(d.side_mu);
+  for (DevInfo::Side *s : d.sides) {
+    if (s->busy) continue;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s->stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) continue;
+    s->busy = true;
+    return s;
+  }
+  DevInfo::Side *s = new (std::nothrow) DevInfo::Side;
+  if (!s) {
+    *err = cudaErrorMemoryAllocation;
+    return nullptr;
+  }
+  cudaError_t e = cudaStreamCreateWithFlags(&s->stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    if (s->join) cudaEventDestroy(s->join);
+    if (s->fork) cudaEventDestroy(s->fork);
+    if (s->stream) cudaStreamDestroy(s->stream);
+    delete s;
+    *err = e;
+    return nullptr;
+  }
+  s->busy = true;
+  d.sides.push_back(s);
+  return s;
+}
+
+void side_release(DevInfo &d, DevInfo::Side *s) {
+  std::lock_guard<std::mutex> lock(d.side_mu);
+  s->busy = false;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -223,7 +283,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 16, 256);
   const int64_t ws_bytes = off_hist + round_up(int64_t(kMaxIters + 1) * 4, 256);
   void *ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)ws_bytes, d->pool, stream);
+  cudaError_t e = pool_alloc(&ws, (size_t)ws_bytes, d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
   char *base = static_cast<char *>(ws);
   uint32_t *amax_part = reinterpret_cast<uint32_t *>(base);
@@ -233,7 +293,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
 
   {
     TraceScope tr(bulk ? kTrAmax : kTrAmaxLdg, stream);
-    e = bulk ? launch_amax_bulk(W, H, amax_part, g_amax, stream)
+    e = bulk ? launch_amax_bulk(W, H, amax_part, g_amax, g_first_wait.load(), stream)
              : launch_amax_partials(W, H, amax_part, g_amax, stream);
   }
   if (e == cudaSuccess && !cjso) {
@@ -283,39 +343,41 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
     // the single-tensor sequence per tensor, tensors alternating between the
     // caller's stream and the library's second one, so that one tensor's
     // sweeps (HBM-bound) can run beside another's search (ALU-bound)
-    std::unique_lock<std::mutex> side_lock(d->side_mu, std::defer_lock);
     cudaError_t e = cudaSuccess;
-    if (count >= 2) {
-      side_lock.lock();
-      e = cudaEventRecord(d->fork, stream);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->side, d->fork, 0);
+    DevInfo::Side *sd = count >= 2 ? side_acquire(*d, &e) : nullptr;
+    if (sd) {
+      e = cudaEventRecord(sd->fork, stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sd->stream, sd->fork, 0);
     }
     for (int i = 0; i < count && e == cudaSuccess && st == NVFP4_OK; ++i) {
       const nvfp4_tensor &x = tensors[i];
       st = nvfp4_quantize(x.W, x.rows, x.cols, mode, iters, x.codes, x.scales, x.alpha,
-                          side_lock.owns_lock() && (i & 1) ? d->side : stream);
+                          sd && (i & 1) ? sd->stream : stream);
     }
-    if (side_lock.owns_lock()) {  // join, also after an error
-      cudaError_t ej = cudaEventRecord(d->join, d->side);
-      if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, d->join, 0);
+    if (sd) {  // join, also after an error
+      cudaError_t ej = cudaEventRecord(sd->join, sd->stream);
+      if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, sd->join, 0);
       if (e == cudaSuccess) e = ej;
+      side_release(*d, sd);
     }
     return st != NVFP4_OK ? st : map_cuda(e);
   }
 
   // Parts of at most kGroupMax tensors, each an amax pass and a quantize pass
-  // over its tiles.  A large group (at least 16 x L2 of bf16) is cut into 8
-  // parts of about equal size that alternate between the caller's stream and
-  // the library's second stream, so one part's amax pass (HBM-bound) runs
-  // beside another's quantize pass (ALU-bound); small groups keep one part
-  // per kGroupMax tensors, which lets the quantize pass re-read from L2 what
-  // the amax pass read last.
+  // over its tiles.  A group of at least kPipeMinL2 x L2 of bf16 is cut into
+  // parts of about kPipePartL2 x L2 that alternate between the caller's stream
+  // and a second stream, so one part's amax pass (HBM-bound) runs beside
+  // another's quantize pass (ALU-bound); smaller groups keep one part per
+  // kGroupMax tensors, which lets the quantize pass re-read from L2 what the
+  // amax pass read last.
   int64_t total = 0;
   for (int i = 0; i < count; ++i) total += tensors[i].rows * tensors[i].cols;
-  const bool pipe = total * 2 >= int64_t(16) * d->l2 && count >= 2;
+  const bool pipe = total * 2 >= int64_t(kPipeMinL2) * d->l2 && count >= 2;
+  const int parts = pipe ? (int)std::max<int64_t>(2, (total * 2 + int64_t(kPipePartL2) * d->l2 / 2) /
+                                                         (int64_t(kPipePartL2) * d->l2))
+                         : 1;
   std::vector<int> cut;  // part k covers tensors [cut[k], cut[k + 1])
   cut.push_back(0);
-  const int parts = pipe ? 8 : 1;
   int64_t acc = 0;
   for (int i = 0; i + 1 < count; ++i) {  // a cut after tensor i where 1/parts of the elements is passed
     acc += tensors[i].rows * tensors[i].cols;
@@ -325,14 +387,13 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
   const int nparts = (int)cut.size() - 1;
   const size_t slot = (size_t)round_up(int64_t(kGroupMax) * 4, 256);
   void *ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, slot * nparts, d->pool, stream);
+  cudaError_t e = pool_alloc(&ws, slot * nparts, d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
   e = cudaMemsetAsync(ws, 0, slot * nparts, stream);  // every tensor's max|W| word starts at 0
-  std::unique_lock<std::mutex> side_lock(d->side_mu, std::defer_lock);
-  if (pipe && e == cudaSuccess) {  // fork the second stream off the caller's
-    side_lock.lock();
-    e = cudaEventRecord(d->fork, stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->side, d->fork, 0);
+  DevInfo::Side *sd = pipe && e == cudaSuccess ? side_acquire(*d, &e) : nullptr;
+  if (sd) {  // fork the second stream off the caller's
+    e = cudaEventRecord(sd->fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sd->stream, sd->fork, 0);
   }
   GroupArgs *g = new (std::nothrow) GroupArgs;
   if (!g && e == cudaSuccess) e = cudaErrorMemoryAllocation;
@@ -340,7 +401,7 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
   const int64_t full = int64_t(d->sms) * std::min(d->occ[kKernGroupAmax], d->occ[kq]);
   for (int k = 0; k < nparts && e == cudaSuccess; ++k) {
     const int s0 = cut[k];
-    cudaStream_t ps = pipe && (k & 1) ? d->side : stream;
+    cudaStream_t ps = sd && (k & 1) ? sd->stream : stream;
     g->count = cut[k + 1] - s0;
     g->tile_begin[0] = 0;
     for (int i = 0; i < g->count; ++i) {
@@ -366,10 +427,11 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
     }
   }
   delete g;
-  if (side_lock.owns_lock()) {  // join: the caller's stream waits for the second stream's parts
-    cudaError_t ej = cudaEventRecord(d->join, d->side);
-    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, d->join, 0);
+  if (sd) {  // join: the caller's stream waits for the second stream's parts
+    cudaError_t ej = cudaEventRecord(sd->join, sd->stream);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(stream, sd->join, 0);
     if (e == cudaSuccess) e = ej;
+    side_release(*d, sd);
   }
   cudaError_t ef = cudaFreeAsync(ws, stream);
   return map_cuda(e != cudaSuccess ? e : ef);
@@ -428,12 +490,14 @@ int nvfp4_gemm(const uint8_t *codes, const uint8_t *scales, const float *alpha, 
   // partial sums of tiles shared by several CTAs meet in a workspace
   const int64_t ny = int64_t(batch) * rows;
   void *ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, gemm_tc_workspace_bytes(rows, cols, batch, d->sms), d->pool, stream);
+  cudaError_t e = pool_alloc(&ws, gemm_tc_workspace_bytes(rows, cols, batch, d->sms), d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
   float *part = static_cast<float *>(ws);
   {
     TraceScope tr(kTrGemmTc, stream);
-    e = launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, d->sms, part, y, stream);
+    const long fw = g_first_wait.load();
+    e = launch_gemm_tc(codes, scales, alpha, rows, cols, x, batch, d->sms, part, y,
+                       fw < 0 ? -1 : (int)std::min<long>(fw, INT32_MAX), stream);
   }
   if (e == cudaSuccess) {
     TraceScope tr(kTrGemmTcReduce, stream);
@@ -497,6 +561,17 @@ int nvfp4_ffma_probe(int packed, int64_t rounds, float *sink, int64_t sink_float
   if (sink_floats < threads) return NVFP4_ERR_INVALID_ARG;
   *fmas = threads * ffma_probe_fmas_per_thread(packed, rounds);
   return map_cuda(launch_ffma_probe(packed, rounds, grid, sink, stream));
+}
+
+int nvfp4_test_fail_allocations(int count) {
+  if (count < 0) return NVFP4_ERR_INVALID_ARG;
+  g_fail_allocs.store(count);
+  return NVFP4_OK;
+}
+
+int nvfp4_test_first_wait_tries(int64_t tries) {
+  g_first_wait.store(tries < 0 ? -1L : (long)std::min<int64_t>(tries, int64_t(1) << 30));
+  return NVFP4_OK;
 }
 
 int nvfp4_profiler_enable(int on) {

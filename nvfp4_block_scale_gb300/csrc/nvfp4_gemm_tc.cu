@@ -158,6 +158,15 @@ __device__ __forceinline__ bool tc_wait(uint32_t mb, uint32_t parity, volatile i
   return false;
 }
 
+// The first wait of a CTA's MMA thread under the test hook: gives up after
+// `tries` tries (0: at once) and raises `fail`.
+__device__ __forceinline__ bool tc_wait_tries(uint32_t mb, uint32_t parity, volatile int *fail, int tries) {
+  for (int it = 0; it < tries; ++it)
+    if (mbar_try(mb, parity)) return true;
+  *fail = 1;
+  return false;
+}
+
 // The same wait without the early exit: used after a failure to let this
 // CTA's own copies and MMAs in flight finish before it leaves.
 __device__ __forceinline__ void tc_drain(uint32_t mb, uint32_t parity) {
@@ -193,6 +202,7 @@ struct TcArgs {
   int maxc;       // workspace slots per tile
   float *ws;      // [tiles][maxc][batch][128] partial sums
   int tma;        // codes and scales by TMA (cmap, smap) rather than per-thread copies
+  int first_tries;  // < 0: normal; else the MMA thread's first wait gives up after this many tries (test hook)
 };
 
 template <int N>
@@ -390,7 +400,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         }
         if ((i & 1) == p) {
           const int st = i % S;
-          if (!tc_wait(tc_smem(&full[st]), (uint32_t)((i / S) & 1), vfail)) break;
+          const bool ready = i == 0 && a.first_tries >= 0
+                                 ? tc_wait_tries(tc_smem(&full[st]), 0u, vfail, a.first_tries)
+                                 : tc_wait(tc_smem(&full[st]), (uint32_t)((i / S) & 1), vfail);
+          if (!ready) break;
           asm volatile("tcgen05.fence::after_thread_sync;");
           const uint64_t so = (uint64_t)((st * C::kStage) >> 4);
           const uint32_t acc_t = tmem + (uint32_t)((seg % C::NB) * 2 + p) * C::kCols;
@@ -628,7 +641,8 @@ size_t gemm_tc_workspace_bytes(int64_t rows, int64_t cols, int batch, int sms) {
 }
 
 cudaError_t launch_gemm_tc(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
-                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, cudaStream_t st) {
+                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, int first_tries,
+                           cudaStream_t st) {
   if (!g_encode) return cudaErrorInitializationError;
   const TcPlan p = tc_plan(rows, cols, sms);
   const int n = gemm_tc_tile_n(batch);
@@ -652,7 +666,7 @@ cudaError_t launch_gemm_tc(const uint8_t *codes, const uint8_t *scales, const fl
   const bool tma = cols % 256 == 0 && rows < (int64_t(1) << 31) && reinterpret_cast<uintptr_t>(codes) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(scales) % 16 == 0 && tc_bytes_map(&cm, codes, rows, cols / 2, 64u) &&
                    tc_bytes_map(&sm, scales, rows, cols / 16, 16u);
-  const TcArgs a = {codes, scales, alpha, rows, cols, batch, p.K, p.T, p.maxc, ws, tma ? 1 : 0};
+  const TcArgs a = {codes, scales, alpha, rows, cols, batch, p.K, p.T, p.maxc, ws, tma ? 1 : 0, first_tries};
   const int grid = (int)p.G;
   cudaError_t e;
   switch (n) {

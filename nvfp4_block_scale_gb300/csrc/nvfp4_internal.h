@@ -31,7 +31,8 @@ struct GroupArgs {
 };
 
 cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
-cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st);
+cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, long first_limit,
+                             cudaStream_t st);
 int amax_bulk_chunks(int64_t n16);
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
@@ -58,7 +59,8 @@ cudaError_t launch_swizzle_scales(const uint8_t *scales, int64_t rows, int64_t k
 int gemm_tc_tile_n(int batch);
 size_t gemm_tc_workspace_bytes(int64_t rows, int64_t cols, int batch, int sms);
 cudaError_t launch_gemm_tc(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t rows,
-                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, cudaStream_t st);
+                           int64_t cols, const void *x, int batch, int sms, float *ws, float *y, int first_tries,
+                           cudaStream_t st);
 cudaError_t launch_gemm_tc_reduce(const float *ws, int64_t rows, int64_t cols, int batch, int sms, float *y,
                                   int grid, cudaStream_t st);
 cudaError_t prepare_gemm_tc_kernels();

@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
 // kAmaxChunk bytes through kAmaxStages shared-memory stages filled by
 // cp.async.bulk (one elected thread issues, an mbarrier counts the bytes);
 // all threads reduce a stage, then it is refilled.  Every mbarrier wait is
-// bounded: on a timeout the CTA waits (bounded) for its copies in flight and
-// writes the partial 0xFFFFFFFF, which makes the quantize kernel's alpha NaN.
+// bounded: on a timeout the CTA waits (bounded, at the normal limit) for its
+// copies in flight and writes the partial 0xFFFFFFFF, which makes the
+// quantize kernel's alpha NaN.
 constexpr int kAmaxStages = 4;
 constexpr int kAmaxChunk = 32768;
 constexpr size_t kAmaxBulkSmem = (size_t)kAmaxStages * kAmaxChunk;
@@ -172,16 +173,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mb, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mb, uint32_t parity, long limit = kSpinLimit) {
   uint32_t done = 0;
-  for (long it = 0; !done && it < kSpinLimit; ++it)
+  for (long it = 0; !done && it < limit; ++it)
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(mb), "r"(parity) : "memory");
   return done != 0;
 }
 
 __global__ void __launch_bounds__(kThreads) k_amax_bulk(const uint4 *__restrict__ W, int64_t n16,
-                                                        uint32_t *__restrict__ part) {
+                                                        uint32_t *__restrict__ part, long first_limit) {
   extern __shared__ __align__(128) uint4 stage[];  // kAmaxStages x kAmaxChunk bytes
   __shared__ __align__(8) uint64_t mbar[kAmaxStages];
   __shared__ uint32_t red[kWarps];
@@ -214,7 +215,9 @@ __global__ void __launch_bounds__(kThreads) k_amax_bulk(const uint4 *__restrict_
   int j = 0;
   for (int64_t ch = blockIdx.x; ch < nch; ch += gridDim.x, ++j) {
     const int st = j % kAmaxStages;
-    const bool arrived = mbar_wait_bounded(smem_addr(&mbar[st]), (uint32_t)((j / kAmaxStages) & 1));
+    // (first_limit < 0: the normal limit; a test hook can make the first wait give up)
+    const bool arrived = mbar_wait_bounded(smem_addr(&mbar[st]), (uint32_t)((j / kAmaxStages) & 1),
+                                           j == 0 && first_limit >= 0 ? first_limit : kSpinLimit);
     if (!__syncthreads_and(arrived)) {
       ok = false;
       break;
@@ -718,7 +721,8 @@ cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int
   return cudaLaunchKernelEx(&cfg, k_amax_partials, static_cast<const uint4 *>(W), n16, part);
 }
 
-cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st) {
+cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int grid, long first_limit,
+                             cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   cfg.dynamicSmemBytes = kAmaxBulkSmem;
   cudaLaunchAttribute attr[1];
@@ -726,7 +730,7 @@ cudaError_t launch_amax_bulk(const void *W, int64_t n16, uint32_t *part, int gri
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_amax_bulk, static_cast<const uint4 *>(W), n16, part);
+  return cudaLaunchKernelEx(&cfg, k_amax_bulk, static_cast<const uint4 *>(W), n16, part, first_limit);
 }
 
 int amax_bulk_chunks(int64_t n16) { return (int)((n16 * 16 + kAmaxChunk - 1) / kAmaxChunk); }

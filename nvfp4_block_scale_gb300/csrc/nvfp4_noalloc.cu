@@ -12,12 +12,15 @@
 // array instead.
 //
 // The array lives in every GPU that loads the library, from load until exit:
-// NVFP4_NOALLOC_SCRATCH_BYTES = 16 KiB = 4096 four-byte slots.  This variant
-// launches one amax CTA per 65,536 elements (one slot each), so it accepts
-// tensors of up to 4096 * 65,536 = 2^28 elements and rejects larger ones on
-// the host.  In host code the array's name is only a host-side stand-in; the
-// device address is fetched once per device with cudaGetSymbolAddress (first
-// call on that device, with that device current) and passed to the kernels.
+// NVFP4_NOALLOC_SCRATCH_BYTES = 16 KiB = 4096 four-byte slots, one per amax
+// CTA.  The amax pass gets a full wave of CTAs (SMs x resident CTAs), and at
+// least one CTA per 65,536 elements, never more than 4096; the size limit
+// 4096 * 65,536 = 2^28 elements keeps that within the slots, and larger
+// tensors are rejected on the host.  In host code the array's name is only a
+// host-side stand-in; the device address is fetched once per device with
+// cudaGetSymbolAddress (first call on that device, with that device current)
+// and passed to the kernels.
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -44,7 +47,7 @@ struct NoAllocDev {
   int status = NVFP4_OK;
   int sms = 0;
   int l2 = 0;
-  int occ_max = 1, occ_fos = 1;
+  int occ_max = 1, occ_fos = 1, occ_amax = 1;
   uint32_t *scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
@@ -82,6 +85,7 @@ int na_device(NoAllocDev **out) {
       d.scratch = static_cast<uint32_t *>(p);
       d.occ_max = max_active_ctas(kKernQuantMax);
       d.occ_fos = max_active_ctas(kKernQuantFos);
+      d.occ_amax = max_active_ctas(kKernAmaxLdg);
       d.status = NVFP4_OK;
     }
     d.ready = true;
@@ -118,9 +122,11 @@ extern "C" int nvfp4_quantize_noalloc(const void *W, int64_t rows, int64_t cols,
   if (n == 0) return na_map(cudaMemsetAsync(alpha, 0, sizeof(float), stream));
 
   const int64_t H = n / 8;
-  // One amax CTA (one 4-byte slot) per 65,536 elements: at most 4096 slots.
-  const int g_amax = (int)((n + kElemsPerAmaxCta - 1) / kElemsPerAmaxCta);
-  if (g_amax > kNoAllocMaxCtas) return NVFP4_ERR_INVALID_ARG;
+  // One 4-byte slot per amax CTA: a full wave, at least one CTA per 65,536
+  // elements, at most 4096 (the size limit above keeps the second term there).
+  const int64_t per_elems = (n + kElemsPerAmaxCta - 1) / kElemsPerAmaxCta;
+  const int64_t wave = na_grid(d->sms, d->occ_amax, H / 8 + 1);  // as nvfp4_quantize sizes it (8 loads per thread)
+  const int g_amax = (int)std::min<int64_t>(kNoAllocMaxCtas, std::max<int64_t>(per_elems, wave));
   const int g_quant = na_grid(d->sms, mode == kModeFourOverSix ? d->occ_fos : d->occ_max, n / 16);
   cudaError_t e = launch_amax_partials(W, H, d->scratch, g_amax, stream);
   const int ranged = 2 * n <= int64_t(d->l2) / 2;

@@ -87,3 +87,59 @@ def test_concurrent_streams_match_sequential_calls():
     torch.cuda.synchronize()
     for (a, b, c), (d, e, f) in zip(seq, conc):
         assert torch.equal(a, d) and torch.equal(b, e) and torch.equal(c, f)
+
+
+def test_grouped_calls_captured_in_one_thread_while_another_thread_calls():
+    """One thread captures grouped calls into a CUDA graph (the CJSO tensor
+    alternation and the two-stream FourOverSix parts both use a second stream)
+    and, before it ends the capture, another thread makes the same kinds of
+    grouped calls uncaptured.  Both must succeed: the uncaptured calls must
+    not land on a second stream that still belongs to the open capture.  The
+    graph's replay and the other thread's results equal eager calls."""
+    import threading
+
+    small = [to_device(synthetic.mlp_up(900 + i, 256, 1024)) for i in range(3)]
+    small_o = [to_device(synthetic.mlp_up(910 + i, 256, 1024)) for i in range(3)]
+    big = [to_device(synthetic.studentt_4k(920 + i, 8192, 12288)) for i in range(3)]  # 576 MiB: two parts
+    big_o = [to_device(synthetic.studentt_4k(930 + i, 8192, 12288)) for i in range(3)]
+    runs = [(small, nv.CJSO, 2), (big, nv.FOUR_OVER_SIX, 0)]
+    runs_o = [(small_o, nv.CJSO, 2), (big_o, nv.FOUR_OVER_SIX, 0)]
+    ref = [nv.quantize_grouped(ws, m, it) for ws, m, it in runs]  # eager; also the one-time set-up
+    ref_o = [nv.quantize_grouped(ws, m, it) for ws, m, it in runs_o]
+    torch.cuda.synchronize()
+    outs = [[tuple(torch.empty_like(t) for t in o) for o in r] for r in ref]
+    outs_o = [[tuple(torch.empty_like(t) for t in o) for o in r] for r in ref_o]
+    captured, done, errors = threading.Event(), threading.Event(), []
+
+    def other_thread():
+        try:
+            assert captured.wait(120)
+            s = torch.cuda.Stream()
+            for (ws, m, it), o in zip(runs_o, outs_o):
+                nv.quantize_grouped(ws, m, it, outs=o, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+        finally:
+            done.set()
+
+    th = threading.Thread(target=other_thread)
+    th.start()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=torch.cuda.Stream(), capture_error_mode="thread_local"):
+            for (ws, m, it), o in zip(runs, outs):
+                nv.quantize_grouped(ws, m, it, outs=o)
+            captured.set()
+            assert done.wait(300)
+    finally:
+        captured.set()
+        th.join()
+    assert not errors, errors
+    g.replay()
+    torch.cuda.synchronize()
+    for got, exp in ((outs, ref), (outs_o, ref_o)):
+        for r_got, r_exp in zip(got, exp):
+            for a, b in zip(r_got, r_exp):
+                for x, y in zip(a, b):
+                    assert torch.equal(x, y)

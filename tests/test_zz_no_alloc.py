@@ -51,3 +51,30 @@ def test_noalloc_matches_quantize_on_two_calls_in_a_row():
         assert torch.equal(codes, ref[0])
         assert torch.equal(scales, ref[1])
         assert alpha.item() == ref[2].item()
+
+
+@pytest.mark.gpu
+def test_noalloc_at_its_size_limit_then_on_a_smaller_tensor():
+    """Exactly NVFP4_NOALLOC_MAX_ELEMS = 2^28 elements (512 MiB of bf16: every
+    scratch slot in use, the last one read), then a smaller tensor whose
+    max|W| is far below the first one's: its call uses fewer slots, so a
+    leftover slot of the first call, if read, would change its alpha.  Both
+    compared with nvfp4_quantize."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device="cuda").manual_seed(90)
+    big = (torch.randn((16384, 16384), generator=g, device="cuda") * 3.0).to(torch.bfloat16)  # 2^28 elements
+    small = (torch.randn((1024, 4096), generator=g, device="cuda") * 0.01).to(torch.bfloat16)
+    for W, mode in ((big, nv.MAX), (small, nv.FOUR_OVER_SIX)):
+        rows, cols = W.shape
+        ref = nv.quantize(W, mode)
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device="cuda")
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device="cuda")
+        alpha = torch.empty((1,), dtype=torch.float32, device="cuda")
+        st = nv.nvfp4_quantize_noalloc(W.data_ptr(), rows, cols, mode, codes.data_ptr(), scales.data_ptr(),
+                                       alpha.data_ptr(), stream.cuda_stream)
+        assert st == 0, nv.nvfp4_status_string(st)
+        torch.cuda.synchronize()
+        assert alpha.item() == ref[2].item()
+        assert torch.equal(codes, ref[0]) and torch.equal(scales, ref[1])
