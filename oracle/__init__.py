@@ -79,6 +79,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_e2m1_value.restype = ctypes.c_double
     L.oracle_e4m3_value.argtypes = [ci]
     L.oracle_e4m3_value.restype = ctypes.c_double
+    L.oracle_u128_to_double.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+    L.oracle_u128_to_double.restype = ctypes.c_double
     L.oracle_bf16_round.argtypes = [p, i64, p]
     L.oracle_bf16_round.restype = None
     L.oracle_block_sums.argtypes = [p, i64, ctypes.c_float, p, p, p, p]
@@ -218,6 +220,11 @@ def e2m1_value(code: int) -> float:
 
 def e4m3_value(code: int) -> float:
     return lib().oracle_e4m3_value(int(code))
+
+
+def u128_to_double(v: int) -> float:
+    """A nonnegative integer below 2^128 rounded to the nearest double (ties to even)."""
+    return lib().oracle_u128_to_double((v >> 64) & (2**64 - 1), v & (2**64 - 1))
 
 
 def bf16_round(v) -> np.ndarray:

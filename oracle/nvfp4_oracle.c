@@ -47,8 +47,9 @@
  *   R7  a block whose dequant scale fl(alpha*Delta) is zero has all code
  *       magnitudes 0 (and P = R = 0).
  *   R8  CJSO: alpha* = sum_i Delta_i P_i / sum_i Delta_i^2 R_i (the printed
- *       form has alpha where Delta_i belongs), summed in double in row-major
- *       block order and rounded to fp32; Delta_i* = e4m3(fl(P_i / fl(alpha R_i))),
+ *       form has alpha where Delta_i belongs), both sums exact (128-bit fixed
+ *       point), each rounded once to double, the quotient taken in double and
+ *       rounded to fp32; Delta_i* = e4m3(fl(P_i / fl(alpha R_i))),
  *       Delta_i kept when R_i = 0; one iteration = alpha step, re-quantize,
  *       Delta step, re-quantize; T = 0 is the max rule.
  *   R9  decoupled: m_k = fl32((50+k)/100), k = 0..100; Delta^q = fl(Delta^d0*m_k);
@@ -384,17 +385,53 @@ static void set_alpha(ctx_t *c, float alpha) {
   c->six_alpha = alpha * 6.0f;
 }
 
-/* [SOAR-A], reading R8: alpha* from the current Delta_i, P_i, R_i, summed in
- * double in row-major block order. Returns the old alpha if the denominator is 0. */
+/* A nonnegative 128-bit integer -> the nearest double (ties to even). */
+static double u128_to_double(unsigned __int128 v) {
+  int h = 127;
+  if (v == 0) return 0.0;
+  while (!((v >> h) & 1)) --h; /* the highest set bit */
+  if (h < 53) return (double)(uint64_t)v;
+  int drop = h - 52; /* bits below a 53-bit significand */
+  unsigned __int128 top = v >> drop;
+  unsigned __int128 rem = v - (top << drop);
+  unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
+  if (rem > half || (rem == half && (top & 1))) top += 1; /* may become 2^53: still exact */
+  return ldexp((double)(uint64_t)top, drop);
+}
+
+/* [SOAR-A], reading R8: alpha* = sum_i Delta_i P_i / sum_i Delta_i^2 R_i from the
+ * current Delta_i, P_i, R_i.  Both sums are formed exactly (so the order of the
+ * blocks does not matter), as nonnegative 128-bit integers:
+ *   Delta_i^2 R_i = M^2 R4 * 2^-20 exactly, with Delta_i = M * 2^-9 and R_i = R4 / 4;
+ *   Delta_i P_i = M mP * 2^(e - 33), with P_i = mP * 2^(e - 24) (mP < 2^24),
+ *   counted in units of 2^U, U = (biased exponent of the alpha the P_i were
+ *   computed with) - 127 - 48; a term's bits below 2^U would be dropped (for
+ *   inputs in range there are none: every P_i is a multiple of about
+ *   2^(exponent of alpha - 33)).
+ * Each sum is rounded once to double, the quotient is taken in double and
+ * rounded to fp32.  Returns alpha_old if the denominator is 0. */
 static float alpha_step(const ctx_t *c, float alpha_old) {
-  double num = 0.0, den = 0.0;
+  uint32_t abits;
+  memcpy(&abits, &alpha_old, 4);
+  const int U = (int)((abits >> 23) & 0xFFu) - 127 - 48;
+  unsigned __int128 num = 0, den = 0;
   for (int64_t b = 0; b < c->nblocks; ++b) {
-    double d = e4m3_value(c->dcode[b]);
-    num += d * (double)c->P[b];
-    den += d * d * (double)c->R[b];
+    const uint64_t M = (uint64_t)ldexp(e4m3_value(c->dcode[b]), 9); /* Delta = M * 2^-9, exactly */
+    const uint64_t R4 = (uint64_t)(c->R[b] * 4.0f);                  /* R = R4 / 4, exactly */
+    den += (unsigned __int128)(M * M) * R4;
+    if (c->P[b] > 0.0f && M > 0) {
+      int e;
+      const float f = frexpf(c->P[b], &e); /* P = f 2^e, f in [0.5, 1) */
+      const uint64_t mP = (uint64_t)ldexpf(f, 24);
+      const unsigned __int128 t = (unsigned __int128)(M * mP);
+      const int sh = e - 33 - U;
+      num += sh >= 0 ? t << sh : t >> -sh;
+    }
   }
-  if (!(den > 0.0)) return alpha_old;
-  return (float)(num / den);
+  if (den == 0) return alpha_old;
+  const double nd = ldexp(u128_to_double(num), U);
+  const double dd = ldexp(u128_to_double(den), -20);
+  return (float)(nd / dd);
 }
 
 static int check_args(const uint16_t *w, int64_t rows, int64_t cols) {
@@ -665,6 +702,11 @@ double oracle_e2m1_value(int code) {
 }
 
 double oracle_e4m3_value(int code) { return e4m3_value(code & 0xFF); }
+
+/* The 128-bit integer hi * 2^64 + lo rounded to the nearest double. */
+double oracle_u128_to_double(uint64_t hi, uint64_t lo) {
+  return u128_to_double(((unsigned __int128)hi << 64) | lo);
+}
 
 void oracle_bf16_round(const float *v, int64_t n, uint16_t *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(v[i]);

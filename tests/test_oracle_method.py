@@ -425,3 +425,102 @@ def test_swizzle_is_a_padded_permutation():
     nz = ids[ids != 0]
     assert np.array_equal(np.sort(nz), np.arange(1, rows * kb + 1))
     assert ids.size == 256 * 8 and (ids == 0).sum() == 256 * 8 - rows * kb
+
+
+# ------------------------------------------------------ exact alpha step
+
+def test_u128_to_double_rounds_to_nearest_even():
+    """The conversion of the exact sums against Python's int -> float, which
+    rounds to nearest with ties to even: random magnitudes, exact ties,
+    values one unit either side of a tie, and carries into the next binade."""
+    rng = np.random.default_rng(21)
+    vals = [0, 1, 2**53 - 1, 2**53, 2**53 + 1, 2**53 + 3, 2**54 + 2, 2**54 + 6, 2**64 - 1, 2**64, 2**128 - 1,
+            (2**53 - 1) * 2**60 + 2**59, (2**53 - 1) * 2**60 + 2**59 - 1, (2**53 - 1) * 2**60 + 2**59 + 1]
+    for _ in range(2000):
+        bits = int(rng.integers(1, 129))
+        v = int(rng.integers(0, 2**63)) | (int(rng.integers(0, 2**63)) << 63) | (int(rng.integers(0, 4)) << 126)
+        vals.append(v & (2**bits - 1))
+        h = int(rng.integers(53, 127))  # an exact tie at bit h - 53
+        t = (int(rng.integers(2**52, 2**53)) << (h - 52)) | (1 << (h - 53))
+        vals += [t, t - 1, t + 1]
+    for v in vals:
+        assert oracle.u128_to_double(v) == float(v), v
+
+
+def exact_alpha(w, codes, scales):
+    """alpha* of the closed form from the exact rationals: sum Delta P and
+    sum Delta^2 R as Python fractions (no rounding), each rounded once to
+    double, the quotient in double, rounded to fp32."""
+    from fractions import Fraction
+    x = np.abs(block_view(w))
+    q = np.abs(code_values(unpack_codes(codes, w.size))).reshape(-1, 16)
+    d = E4M3_VALUES[scales.reshape(-1)]
+    num, den = Fraction(0), Fraction(0)
+    for xb, qb, db in zip(x, q, d):
+        if db == 0.0:
+            continue
+        P = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(xb, qb))
+        R = sum(Fraction(float(b)) ** 2 for b in qb)
+        num += Fraction(float(db)) * P
+        den += Fraction(float(db)) ** 2 * R
+    return float(np.float32(float(num) / float(den)))
+
+
+def wide_range_tensor():
+    """N(0, 1e-5) with one element 1.0: most block scales are E4M3 subnormals
+    and most terms Delta P lie ~2^-30 below alpha, so any loss of low bits in
+    the sums shows in alpha."""
+    a = synthetic.bits_to_f32(synthetic.gaussian(16, 512, 1e-5, 35)).copy()
+    a[3, 77] = 1.0
+    return synthetic.to_bf16_bits(a)
+
+
+@pytest.mark.parametrize("make", [lambda: synthetic.mlp_up(31, 16, 512), lambda: synthetic.student_t(8, 1024, 4.0, 0.02, 32),
+                                  lambda: synthetic.mlp_70b(33, 16, 512), wide_range_tensor])
+def test_cjso_alpha_is_the_exact_closed_form(make):
+    """alpha after each CJSO iteration equals the closed form evaluated on
+    exact sums (Python fractions), whatever the block order."""
+    w = make()
+    for T in (0, 1, 2):
+        codes, scales, _ = oracle.quantize(w, oracle.CJSO, T)
+        _, _, a_next = oracle.quantize(w, oracle.CJSO, T + 1)
+        assert a_next == exact_alpha(w, codes, scales)
+    # the blocks in another order (rows reversed): the same alpha
+    _, _, a = oracle.quantize(w, oracle.CJSO, 2)
+    _, _, b = oracle.quantize(np.ascontiguousarray(w[::-1]), oracle.CJSO, 2)
+    assert a == b
+
+
+def tie_tensor(extra_half_codes: int):
+    """A tensor whose first CJSO alpha step lands exactly on an fp32 midpoint
+    (extra_half_codes = 0), or one quarter of R below or above it (+1 / -1).
+
+    alpha0 = 2^-12 (global max 0.65625 = 2688 * 2^-12).  Every block is
+    exactly representable on its max-rule scale (x = q * Delta * alpha0, so
+    Delta P = alpha0 Delta^2 R) except block B = [y, 0, ...]: y = 1.5078125 *
+    2^-4 has scale Delta = 64 and code 6, and 6y exceeds 36 alpha0 Delta by
+    eps = 3 * 2^-10.  Hence alpha1 = alpha0 + Delta eps / den with den =
+    sum Delta^2 R; filler blocks of scale 64 make den = 3 * 2^32 exactly, and
+    alpha1 = 2^-12 + 2^-36: halfway between 2^-12 and 2^-12 + 2^-35.  One more
+    (one fewer) element of code 0.5 raises (lowers) den by 1024 and moves
+    alpha1 just below (above) the midpoint."""
+    u = 2.0 ** -6  # alpha0 * 64
+    blocks = [[0.65625] + [0.0] * 15, [1.5078125 * 2.0 ** -4] + [0.0] * 15]
+    blocks += [[6 * u] * 16] * 5458
+    special = [6 * u] * 3 + [3 * u, 1.5 * u] + [0.5 * u] * (3 + extra_half_codes)
+    blocks.append(special + [0.0] * (16 - len(special)))
+    blocks += [[0.0] * 16] * (5504 - len(blocks))
+    a = np.array(blocks, np.float32).reshape(128, 688)
+    sign = np.where(np.random.default_rng(34).random(a.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    return synthetic.to_bf16_bits(a * sign)
+
+
+@pytest.mark.parametrize("extra,expect", [(0, 2.0 ** -12), (1, 2.0 ** -12), (-1, 2.0 ** -12 + 2.0 ** -35)])
+def test_cjso_alpha_on_an_fp32_midpoint(extra, expect):
+    """The first alpha step of the constructed tensors: exactly on a midpoint
+    (ties to the even neighbour 2^-12), a hair below, a hair above."""
+    w = tie_tensor(extra)
+    _, _, a0 = oracle.quantize(w, oracle.MAX)
+    assert a0 == 2.0 ** -12
+    _, _, a1 = oracle.quantize(w, oracle.CJSO, 1)
+    assert a1 == expect

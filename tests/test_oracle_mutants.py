@@ -58,8 +58,12 @@ MUTANTS = [
     ("fos_error_compares_scale_of_m6", "float g4 = cand_err(c->alpha * delta4, P4, R4);",
      "float g4 = cand_err(c->alpha * delta6, P4, R4);"),
     # CJSO
-    ("alpha_den_printed_form", "den += d * d * (double)c->R[b];", "den += d * (double)c->R[b];"),
-    ("alpha_num_dropped_delta", "num += d * (double)c->P[b];", "num += (double)c->P[b];"),
+    ("alpha_den_printed_form", "den += (unsigned __int128)(M * M) * R4;", "den += (unsigned __int128)(M * 512) * R4;"),
+    ("alpha_num_dropped_delta", "const unsigned __int128 t = (unsigned __int128)(M * mP);",
+     "const unsigned __int128 t = (unsigned __int128)(512 * mP);"),
+    ("alpha_sum_units_too_coarse", "0xFFu) - 127 - 48;", "0xFFu) - 127 - 8;"),
+    ("alpha_sum_rounds_half_up", "if (rem > half || (rem == half && (top & 1))) top += 1;", "if (rem >= half) top += 1;"),
+    ("alpha_quotient_in_float", "return (float)(nd / dd);", "return (float)nd / (float)dd;"),
     ("delta_step_transposed", "float t = P / (c->alpha * R);", "float t = R / (c->alpha * P);"),
     ("delta_step_dropped_alpha", "float t = P / (c->alpha * R);", "float t = P / R;"),
     ("delta_step_without_requantize",
