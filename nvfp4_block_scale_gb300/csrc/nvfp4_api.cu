@@ -278,17 +278,17 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
-  // scratch: amax partials | 2 x CJSO partial sums | alpha history
+  // scratch: amax partials | 2 x CJSO partial sums (two 128-bit integers per CTA) | alpha history
   const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);
-  const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 16, 256);
+  const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 32, 256);
   const int64_t ws_bytes = off_hist + round_up(int64_t(kMaxIters + 1) * 4, 256);
   void *ws = nullptr;
   cudaError_t e = pool_alloc(&ws, (size_t)ws_bytes, d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
   char *base = static_cast<char *>(ws);
   uint32_t *amax_part = reinterpret_cast<uint32_t *>(base);
-  float4 *part[2] = {reinterpret_cast<float4 *>(base + off_part),
-                     reinterpret_cast<float4 *>(base + off_part) + g_cjso};
+  ulonglong2 *part[2] = {reinterpret_cast<ulonglong2 *>(base + off_part),
+                         reinterpret_cast<ulonglong2 *>(base + off_part) + 2 * int64_t(g_cjso)};
   float *hist = reinterpret_cast<float *>(base + off_hist);
 
   {

@@ -344,26 +344,4 @@ __device__ __forceinline__ float cand_err_m2p(float s, float m2P, float R) {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Compensated (float, float) accumulator, ~48 significant bits.
-struct FF {
-  float hi, lo;
-};
-
-__device__ __forceinline__ void ff_add(FF &a, float bh, float bl) {
-  float s = __fadd_rn(a.hi, bh);
-  float bp = __fsub_rn(s, a.hi);
-  float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(bh, bp));
-  float lo = __fadd_rn(a.lo, __fadd_rn(e, bl));
-  float t = __fadd_rn(s, lo);
-  a.lo = __fsub_rn(lo, __fsub_rn(t, s));
-  a.hi = t;
-}
-
-// Adds the exact product x*y (two-product via fma).
-__device__ __forceinline__ void ff_add_prod(FF &a, float x, float y) {
-  float p = __fmul_rn(x, y);
-  float pe = __fmaf_rn(x, y, -p);
-  ff_add(a, p, pe);
-}
-
 }  // namespace nvfp4

@@ -38,7 +38,7 @@ cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint3
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
                                  cudaStream_t st);
 cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
-                       const float4 *part_in, int n_in, float4 *part_out, float *alpha_hist, int t,
+                       const ulonglong2 *part_in, int n_in, ulonglong2 *part_out, float *alpha_hist, int t,
                        uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                        int grid, cudaStream_t st);
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,

@@ -46,33 +46,83 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
   return r;
 }
 
-__device__ __forceinline__ void warp_ff_sum(FF &a) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float h = __shfl_xor_sync(0xFFFFFFFFu, a.hi, o);
-    float l = __shfl_xor_sync(0xFFFFFFFFu, a.lo, o);
-    ff_add(a, h, l);
-  }
+typedef unsigned __int128 u128;
+
+__device__ __forceinline__ u128 shfl_xor_u128(u128 v, int o) {
+  const uint64_t lo = __shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)v, o);
+  const uint64_t hi = __shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)(v >> 64), o);
+  return ((u128)hi << 64) | lo;
 }
 
-// Sums two compensated accumulators over the CTA in a fixed order; the
-// result is valid in thread 0.
-__device__ __forceinline__ void block_ff_sum2(FF &a, FF &b, float4 *red) {
-  warp_ff_sum(a);
-  warp_ff_sum(b);
+// Sums two 128-bit integers over the CTA (exact, so the order is immaterial);
+// the result is valid in thread 0.
+__device__ __forceinline__ void block_sum2_u128(u128 &a, u128 &b, ulonglong2 *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += shfl_xor_u128(a, o);
+    b += shfl_xor_u128(b, o);
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) red[warp] = make_float4(a.hi, a.lo, b.hi, b.lo);
+  if (lane == 0) {
+    red[2 * warp] = make_ulonglong2((unsigned long long)a, (unsigned long long)(a >> 64));
+    red[2 * warp + 1] = make_ulonglong2((unsigned long long)b, (unsigned long long)(b >> 64));
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    FF x = {0.0f, 0.0f}, y = {0.0f, 0.0f};
+    u128 x = 0, y = 0;
     for (int w = 0; w < kWarps; ++w) {
-      ff_add(x, red[w].x, red[w].y);
-      ff_add(y, red[w].z, red[w].w);
+      x += ((u128)red[2 * w].y << 64) | red[2 * w].x;
+      y += ((u128)red[2 * w + 1].y << 64) | red[2 * w + 1].x;
     }
     a = x;
     b = y;
   }
   __syncthreads();
+}
+
+// A nonnegative 128-bit integer -> the nearest double, ties to the even one.
+__device__ __forceinline__ double u128_to_double_rne(u128 v) {
+  const uint64_t hi = (uint64_t)(v >> 64), lo = (uint64_t)v;
+  const int h = hi ? 127 - __clzll((long long)hi) : (lo ? 63 - __clzll((long long)lo) : -1);
+  if (h < 53) return (double)lo;  // exact
+  const int drop = h - 52;
+  uint64_t top = (uint64_t)(v >> drop);  // 53 bits
+  const u128 rest = v & (((u128)1 << drop) - 1);
+  const u128 half = (u128)1 << (drop - 1);
+  if (rest > half || (rest == half && (top & 1u))) top += 1;  // 2^53 at most: still exact
+  return ldexp((double)top, drop);
+}
+
+// A 128-bit accumulator as two 64-bit words (added with carries by hand:
+// cheaper than the compiler's 128-bit arithmetic on the hot path).
+struct Acc128 {
+  uint64_t lo = 0, hi = 0;
+  __device__ __forceinline__ void add(uint64_t l, uint64_t h) {
+    lo += l;
+    hi += h + (lo < l ? 1u : 0u);
+  }
+  __device__ __forceinline__ u128 get() const { return ((u128)hi << 64) | lo; }
+};
+
+// The exact terms of [SOAR-A]'s sums for one block: Delta^2 R in units of
+// 2^-20 (Delta = M 2^-9, R = R4 / 4) and Delta P in units of 2^U, P the exact
+// fp32 sum (bits below 2^U, which in-range inputs never have, are dropped).
+__device__ __forceinline__ void alpha_terms(uint32_t M, float P, float R, int U, Acc128 &num, Acc128 &den) {
+  const uint32_t R4 = __float2uint_rz(__fmul_rn(R, 4.0f));
+  den.add((uint64_t)M * M * R4, 0u);  // < 2^48
+  const uint32_t pb = __float_as_uint(P);
+  if (P > 0.0f && M > 0u) {
+    const uint32_t e = pb >> 23;
+    const uint64_t mP = e ? (pb & 0x7FFFFFu) | 0x800000u : (pb & 0x7FFFFFu);  // P = mP 2^(max(e,1) - 150)
+    const int sh = (int)(e ? e : 1u) - 150 - 9 - U;
+    const uint64_t tv = (uint64_t)M * mP;  // < 2^42
+    if (sh >= 0 && sh < 64) {              // the usual case
+      num.add(tv << sh, sh ? tv >> (64 - sh) : 0u);
+    } else {
+      const u128 v = sh >= 0 ? (u128)tv << sh : (u128)tv >> (-sh);
+      num.add((uint64_t)v, (uint64_t)(v >> 64));
+    }
+  }
 }
 
 // [SOAR-Q] alpha = max|W| / (6*448), from the per-CTA amax partials.
@@ -352,19 +402,36 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
 // waits for the previous sweep before reading the partials and the scales.
 // `descending` alternates between sweeps so that each starts on the part of
 // W the previous one read last (still in L2 when W is larger than L2).
+// One sweep over all blocks, one block per thread.  INIT: max rule from the
+// amax partials.  Otherwise: alpha from the previous sweep's partial sums
+// ([SOAR-A]), sums with the stored Delta, Delta* ([SOAR-D]) rounded to E4M3,
+// re-quantize ([SOAR-SCHED]).  Every sweep stores Delta, writes its CTA's
+// partial sums sum Delta P and sum Delta^2 R (exact 128-bit integers: Delta P
+// in units of 2^U with U = the exponent of the sweep's alpha - 48, Delta^2 R
+// in units of 2^-20), and records alpha in alpha_hist[t]; the next sweep adds
+// all partials exactly, rounds each sum once to double and takes the quotient
+// in double, so alpha does not depend on the order of the blocks.  Sweeps
+// chain by programmatic dependent launch: each prefetches its first blocks of
+// W (an input, final before the chain began) and then waits for the previous
+// sweep before reading the partials and the scales.  `descending` alternates
+// between sweeps so that each starts on the part of W the previous one read
+// last (still in L2 when W is larger than L2).
+__device__ __forceinline__ int alpha_unit(float alpha) { return (int)((__float_as_uint(alpha) >> 23) & 0xFFu) - 127 - 48; }
+
 template <bool INIT>
 __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict__ W, int64_t B,
                                                          const uint32_t *__restrict__ amax_part, int n_amax,
-                                                         const float4 *__restrict__ part_in, int n_in,
-                                                         float4 *__restrict__ part_out,
+                                                         const ulonglong2 *__restrict__ part_in, int n_in,
+                                                         ulonglong2 *__restrict__ part_out,
                                                          float *__restrict__ alpha_hist, int t,
                                                          uint8_t *__restrict__ scales,
                                                          uint32_t *__restrict__ codes32, int write_codes,
                                                          float *__restrict__ alpha_out, int write_alpha,
                                                          int descending) {
   __shared__ uint32_t red[kWarps];
-  __shared__ float4 redf[kWarps];
+  __shared__ ulonglong2 redu[2 * kWarps];
   __shared__ float s_tab[128], r_tab[128], ev_tab[128];
+  __shared__ uint32_t m_tab[128];  // E4M3 value * 2^9
   __shared__ float sh_alpha;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -374,7 +441,11 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   auto ok = [&](int64_t x) { return x >= 0 && x < B; };
   uint4 a0 = ok(b) ? __ldg(W + 2 * b) : z, a1 = ok(b) ? __ldg(W + 2 * b + 1) : z;
   uint4 n0 = ok(b + step) ? __ldg(W + 2 * (b + step)) : z, n1 = ok(b + step) ? __ldg(W + 2 * (b + step) + 1) : z;
-  if (threadIdx.x < 128) ev_tab[threadIdx.x] = e4m3_value(threadIdx.x);
+  if (threadIdx.x < 128) {
+    const float ev = e4m3_value(threadIdx.x);
+    ev_tab[threadIdx.x] = ev;
+    m_tab[threadIdx.x] = __float2uint_rz(__fmul_rn(ev, 512.0f));
+  }
 
   pdl_launch_dependents();
   pdl_wait();
@@ -382,17 +453,22 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   if (INIT) {
     alpha = fold_alpha(amax_part, n_amax, red);
   } else {
-    FF num = {0.0f, 0.0f}, den = {0.0f, 0.0f};
+    u128 num = 0, den = 0;
     for (int i = threadIdx.x; i < n_in; i += kThreads) {
-      float4 p = part_in[i];
-      ff_add(num, p.x, p.y);
-      ff_add(den, p.z, p.w);
+      const ulonglong2 pn = part_in[2 * i], pd = part_in[2 * i + 1];
+      num += ((u128)pn.y << 64) | pn.x;
+      den += ((u128)pd.y << 64) | pd.x;
     }
-    block_ff_sum2(num, den, redf);
+    block_sum2_u128(num, den, redu);
     if (threadIdx.x == 0) {
-      const double dn = (double)num.hi + (double)num.lo;
-      const double dd = (double)den.hi + (double)den.lo;
-      sh_alpha = dd > 0.0 ? __double2float_rn(__ddiv_rn(dn, dd)) : alpha_hist[t - 1];
+      const float prev = alpha_hist[t - 1];  // the alpha the partial sums were formed with
+      if (den == 0) {
+        sh_alpha = prev;
+      } else {
+        const double dn = ldexp(u128_to_double_rne(num), alpha_unit(prev));
+        const double dd = ldexp(u128_to_double_rne(den), -20);
+        sh_alpha = __double2float_rn(__ddiv_rn(dn, dd));
+      }
     }
     __syncthreads();
     alpha = sh_alpha;
@@ -403,21 +479,22 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   }
   const float six_a = __fmul_rn(alpha, 6.0f);
   const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
+  const int U = alpha_unit(alpha);
   build_scale_tables(alpha, s_tab, r_tab);
   __syncthreads();
 
-  FF num = {0.0f, 0.0f}, den = {0.0f, 0.0f};
+  Acc128 num_acc, den_acc;
   for (; ok(b); b += step) {
     const int64_t b2 = b + 2 * step;
     const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
-    uint32_t d;
+    uint32_t d, d_old = 0xFFu;
     float P, R;
     if (INIT) {
       d = max_rule_code(am, six_a, r6);
     } else {
-      d = scales[b];
+      d = d_old = scales[b];
       block_sums(blk, s_tab[d], r_tab[d], P, R);
       if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
     }
@@ -426,20 +503,22 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
       quant16<true>(blk, s_tab[d], r_tab[d], c0, c1, P, R);
       codes32[2 * b] = c0;
       codes32[2 * b + 1] = c1;
-    } else {
+    } else if (d != d_old) {  // an unchanged Delta re-quantizes to the same codes, P and R
       block_sums(blk, s_tab[d], r_tab[d], P, R);
     }
     scales[b] = (uint8_t)d;
-    const float dv = ev_tab[d];
-    ff_add_prod(num, dv, P);                             // exact product, compensated sum
-    ff_add(den, __fmul_rn(__fmul_rn(dv, dv), R), 0.0f);  // Delta^2 * R is exact in fp32
+    alpha_terms(m_tab[d], P, R, U, num_acc, den_acc);
     a0 = n0;
     a1 = n1;
     n0 = m0;
     n1 = m1;
   }
-  block_ff_sum2(num, den, redf);
-  if (threadIdx.x == 0) part_out[blockIdx.x] = make_float4(num.hi, num.lo, den.hi, den.lo);
+  u128 num = num_acc.get(), den = den_acc.get();
+  block_sum2_u128(num, den, redu);
+  if (threadIdx.x == 0) {
+    part_out[2 * blockIdx.x] = make_ulonglong2((unsigned long long)num, (unsigned long long)(num >> 64));
+    part_out[2 * blockIdx.x + 1] = make_ulonglong2((unsigned long long)den, (unsigned long long)(den >> 64));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -754,7 +833,7 @@ cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint3
 }
 
 cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
-                              const float4 *part_in, int n_in, float4 *part_out, float *alpha_hist, int t,
+                              const ulonglong2 *part_in, int n_in, ulonglong2 *part_out, float *alpha_hist, int t,
                               uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                               int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);

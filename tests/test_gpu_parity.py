@@ -131,3 +131,20 @@ def test_dequant_of_every_code_and_scale():
     for a in (2.0 ** -12, 1.2345e-5, 0.0):
         od = oracle.dequantize(codes, scales, a, rows, cols)
         assert np.array_equal(gpu_dequantize(codes, scales, a, rows, cols), od)
+
+
+@pytest.mark.parametrize("extra,expect", [(0, 2.0 ** -12), (1, 2.0 ** -12), (-1, 2.0 ** -12 + 2.0 ** -35)])
+def test_cjso_alpha_on_an_fp32_midpoint(extra, expect):
+    """Tensors whose first CJSO alpha step lands exactly on an fp32 midpoint,
+    a hair below it and a hair above it (constructed in the oracle's pins):
+    the device's exact 128-bit sums give the same alpha as the oracle and as
+    the arithmetic, and every block agrees, for CJSO(1) and CJSO(3)."""
+    from test_oracle_method import tie_tensor
+    w = tie_tensor(extra)
+    gc, gs, ga = gpu_quantize(w, oracle.CJSO, 1)
+    assert ga == expect
+    for iters in (1, 3):
+        gc, gs, ga = gpu_quantize(w, oracle.CJSO, iters)
+        oc, os_, oa = oracle.quantize(w, oracle.CJSO, iters)
+        assert ga == oa
+        assert np.array_equal(gc, oc) and np.array_equal(gs, os_)
