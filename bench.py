@@ -86,8 +86,9 @@ DECOUPLED_FLOPS = 101 * 5  # per element: 101 candidates x (quotient FMUL 1 + P 
 
 def kernels_per_call(mode: int, iters: int) -> int:
     """Kernels one call launches: amax + quantize; amax + init sweep + one
-    sweep per iteration (+ the search); one kernel for the consumers."""
-    return {0: 2, 1: 2, 2: 2 + iters, 3: 3 + iters, 4: 1, 5: 1, 6: 1, 7: 2, 8: 2, 9: 2}[mode]
+    sweep per iteration (+ the search and its deferred-block pass); one kernel
+    for the consumers."""
+    return {0: 2, 1: 2, 2: 2 + iters, 3: 4 + iters, 4: 1, 5: 1, 6: 1, 7: 2, 8: 2, 9: 2}[mode]
 
 
 def algorithmic(mode: int, iters: int, n: int, l2_bytes: int, batch: int = 1, hbm_gbs: float = 6660.0,

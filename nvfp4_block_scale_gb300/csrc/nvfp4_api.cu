@@ -278,10 +278,13 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   const int ranged = 2 * n <= int64_t(d->l2) / 2;  // W stays in L2 between the two passes
   const int g_quant = grid_for(*d, mode == kModeFourOverSix ? kKernQuantFos : kKernQuantMax, B);
   const int g_cjso = grid_for(*d, kKernCjso, B);
-  // scratch: amax partials | 2 x CJSO partial sums (two 128-bit integers per CTA) | alpha history
+  // scratch: amax partials | 2 x CJSO partial sums (two 128-bit integers per CTA) | alpha history |
+  // (decoupled) the count and list of the search's deferred blocks
   const int64_t off_part = round_up(int64_t(g_amax) * 4, 256);
   const int64_t off_hist = off_part + round_up(2 * int64_t(g_cjso) * 32, 256);
-  const int64_t ws_bytes = off_hist + round_up(int64_t(kMaxIters + 1) * 4, 256);
+  const int64_t off_defer = off_hist + round_up(int64_t(kMaxIters + 1) * 4, 256);
+  const int defer_cap = (int)std::min<int64_t>(kDeferCap, B);
+  const int64_t ws_bytes = off_defer + (mode == kModeCjsoDecoupled ? 256 + round_up(int64_t(defer_cap) * 8, 256) : 0);
   void *ws = nullptr;
   cudaError_t e = pool_alloc(&ws, (size_t)ws_bytes, d->pool, stream);
   if (e != cudaSuccess) return map_cuda(e);
@@ -290,8 +293,11 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
   ulonglong2 *part[2] = {reinterpret_cast<ulonglong2 *>(base + off_part),
                          reinterpret_cast<ulonglong2 *>(base + off_part) + 2 * int64_t(g_cjso)};
   float *hist = reinterpret_cast<float *>(base + off_hist);
+  uint32_t *defer_count = reinterpret_cast<uint32_t *>(base + off_defer);
+  int64_t *defer_list = reinterpret_cast<int64_t *>(base + off_defer + 256);
 
-  {
+  if (mode == kModeCjsoDecoupled) e = cudaMemsetAsync(defer_count, 0, sizeof(uint32_t), stream);
+  if (e == cudaSuccess) {
     TraceScope tr(bulk ? kTrAmax : kTrAmaxLdg, stream);
     e = bulk ? launch_amax_bulk(W, H, amax_part, g_amax, g_first_wait.load(), stream)
              : launch_amax_partials(W, H, amax_part, g_amax, stream);
@@ -313,7 +319,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
     }
     if (e == cudaSuccess && !plain) {
       TraceScope tr(kTrDecoupled, stream);
-      e = launch_decoupled(W, B, hist, T, scales, codes, d->sms, stream);
+      e = launch_decoupled(W, B, hist, T, scales, codes, defer_count, defer_list, defer_cap, d->sms, stream);
     }
   }
   // The scratch goes back to the pool in stream order, after the last kernel.

@@ -23,7 +23,7 @@
 // decision point b between codes i and i+1 at about kappa = 100 |x| / (b
 // s50) - 50 (s50 = fl(alpha Delta^d0)); kappa computed in fp32 is within
 // 8e-5 of the true crossing (error bound below), so K = ceil(kappa) is the
-// first k with the lower code unless kappa lies within 2^-12 of an integer
+// first k with the lower code unless kappa lies within 2^-13 of an integer
 // (never seen on the benchmark tensors; such a block takes the plain loop
 // below).  Each crossing
 // adds its exact change of P and R to a per-thread shared-memory slot at K
@@ -37,11 +37,12 @@
 // Error bound of kappa: sq_k = alpha Delta^d0 (50+k)/100 (1 + theta), |theta|
 // <= 3 u (u = 2^-24: m_k, the product with Delta^d0, the product with
 // alpha), s50 carries one more u, and the code changes where fl(|x|/sq_k)
-// crosses b, i.e. where |x|/sq_k is within u b of b; the true crossing k is
-// 100 V / b (1 + lambda) - 50 with V = |x| / s50, |lambda| <= 5u, i.e. within
-// 150 * 5u = 4.5e-5.  kappa = fl(fl(|x| fl(1/s50)) * fl(100/b) - 50) carries
-// at most 3u relative on the product (<= 150) and one rounding of a value <=
-// 100: 3.3e-5.  Total < 8e-5, against the 2^-12 = 2.4e-4 margin.
+// crosses b, i.e. where |x|/sq_k is within u b of b (half an fp32 spacing
+// around each b is below u b); the true crossing k is 100 V / b (1 + lambda)
+// - 50 with V = |x| / s50, |lambda| <= 5u, i.e. within 150 * 5u = 4.47e-5.
+// kappa = fl(fl(|x| fl(1/s50)) * fl(100/b) - 50) carries at most 3u relative
+// on the product (<= 150) and one rounding of a value <= 100: 3.28e-5.
+// Total 7.75e-5, against the 2^-13 = 1.22e-4 margin.
 //
 // Exactness of P: with 2^E chosen so that max|x| 2^E < 2^15, X = |x| 2^E is
 // an integer for every element of magnitude >= 2^(7-E); every element whose
@@ -62,9 +63,10 @@
 namespace nvfp4 {
 
 constexpr int kDecThreads = 512;
+constexpr int kPlainThreads = 256;
 constexpr int kDecK = 101;
 constexpr int kSlotK = 100;  // k = 1..100 (k = 0 is the start state)
-constexpr float kAmbig = 0x1p-12f;
+constexpr float kAmbig = 0x1p-13f;
 
 // Dynamic shared memory: per-thread event slots and breakpoint masks, then
 // the per-CTA tables.
@@ -152,7 +154,9 @@ __device__ __forceinline__ float elem(const Block16 &blk, int j) {
 __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__restrict__ W, int64_t B,
                                                               const float *__restrict__ alpha_hist, int t,
                                                               uint8_t *__restrict__ scales,
-                                                              uint32_t *__restrict__ codes32) {
+                                                              uint32_t *__restrict__ codes32,
+                                                              uint32_t *__restrict__ defer_count,
+                                                              int64_t *__restrict__ defer_list, int defer_cap) {
   extern __shared__ __align__(16) unsigned char dsm[];
   uint32_t *slot = reinterpret_cast<uint32_t *>(dsm);            // [k - 1][thread]
   uint32_t *mask = reinterpret_cast<uint32_t *>(dsm + kOffMask);  // [word][thread]
@@ -329,8 +333,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
         }
       }
     }
+    // a block for the plain loop goes to the deferred list (k_decoupled_plain
+    // searches it after this kernel), or, when the list is full, is searched here
+    bool deferred = false;
+    if (path == 2) {
+      const uint32_t slot_i = atomicAdd(defer_count, 1u);
+      if ((int64_t)slot_i < (int64_t)defer_cap) {
+        defer_list[slot_i] = b;
+        deferred = true;
+      }
+    }
     __syncwarp();
-    if (path == 2) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
+    if (path == 2 && !deferred) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
     __syncwarp();
     const int bk = best_i >> 1;
     const uint32_t lb = lo_tab[d0 * kDecK + bk];
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
     const float rq = sq > 0.0f ? __frcp_rn(sq) : 0.0f;  // zero scale: signs only
     const uint32_t c0 = quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[0]), sq, rq);
     const uint32_t c1 = quant8(*reinterpret_cast<const f32x2(*)[4]>(&blk.x[4]), sq, rq);
-    if (live) {
+    if (live && !deferred) {  // a deferred block keeps Delta^d0 in scales[b] for the second kernel
       codes32[2 * b] = c0;
       codes32[2 * b + 1] = c1;
       scales[b] = (uint8_t)best_d;
@@ -349,8 +363,60 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   }
 }
 
+// The deferred blocks of k_decoupled (a crossing too close to an integer k,
+// or a block outside the exact-integer range): the plain search, one block
+// per thread.  Launched as a programmatic dependent of k_decoupled; waits for
+// it before reading the list.
+__global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *__restrict__ W,
+                                                                   const float *__restrict__ alpha_hist, int t,
+                                                                   uint8_t *__restrict__ scales,
+                                                                   uint32_t *__restrict__ codes32,
+                                                                   const uint32_t *__restrict__ defer_count,
+                                                                   const int64_t *__restrict__ defer_list,
+                                                                   int defer_cap) {
+  __shared__ float ev_tab[128], m_tab[kDecK];
+  __shared__ float2 s2_tab[128];
+  __shared__ uint8_t lo_tab[128 * kDecK];
+  const int tid = threadIdx.x;
+  if (tid < 128) ev_tab[tid] = e4m3_value(tid);
+  if (tid < kDecK) m_tab[tid] = __double2float_rn(__ddiv_rn((double)(50 + tid), 100.0));
+  __syncthreads();
+  for (int e = tid; e < 128 * kDecK; e += kPlainThreads) {
+    const int c = e / kDecK, k = e - c * kDecK;
+    lo_tab[e] = (uint8_t)bracket_byte(__fmul_rn(ev_tab[c], m_tab[k]), ev_tab);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  const float alpha = alpha_hist[t];
+  if (tid < 128) {
+    const float sv = __fmul_rn(alpha, ev_tab[tid]);
+    s2_tab[tid] = make_float2(sv, tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f);
+  }
+  __syncthreads();
+  const int64_t n = min((int64_t)*defer_count, (int64_t)defer_cap);
+  for (int64_t i = (int64_t)blockIdx.x * kPlainThreads + tid; i < n; i += (int64_t)gridDim.x * kPlainThreads) {
+    const int64_t b = defer_list[i];
+    const uint32_t d0 = scales[b];
+    const float ev0 = ev_tab[d0];
+    const int best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
+    const int bk = best_i >> 1;
+    const uint32_t lb = lo_tab[d0 * kDecK + bk];
+    const uint32_t best_d = (lb & 0x7Fu) + ((best_i & 1) ? (lb >> 7) : 0u);
+    const float sq = __fmul_rn(alpha, __fmul_rn(ev0, m_tab[bk]));
+    Block16 blk;
+    unpack16(__ldg(W + 2 * b), __ldg(W + 2 * b + 1), blk);
+    uint32_t c0, c1;
+    float P_unused, R_unused;
+    quant16<false>(blk, sq, sq > 0.0f ? __frcp_rn(sq) : 0.0f, c0, c1, P_unused, R_unused);
+    codes32[2 * b] = c0;
+    codes32[2 * b + 1] = c1;
+    scales[b] = (uint8_t)best_d;
+  }
+}
+
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales,
-                             uint8_t *codes, int sms, cudaStream_t st) {
+                             uint8_t *codes, uint32_t *defer_count, int64_t *defer_list, int defer_cap, int sms,
+                             cudaStream_t st) {
   const int64_t need = (B + kDecThreads - 1) / kDecThreads;
   const int grid = (int)(need < sms ? (need < 1 ? 1 : need) : sms);
   cudaLaunchConfig_t cfg = {};
@@ -363,8 +429,17 @@ cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decoupled, static_cast<const uint4 *>(W), B, alpha_hist, t, scales,
-                            reinterpret_cast<uint32_t *>(codes));
+  const uint4 *w = static_cast<const uint4 *>(W);
+  uint32_t *c = reinterpret_cast<uint32_t *>(codes);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_decoupled, w, B, alpha_hist, t, scales, c, defer_count, defer_list,
+                                     defer_cap);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(kPlainThreads);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, k_decoupled_plain, w, static_cast<const float *>(alpha_hist), t, scales, c,
+                            static_cast<const uint32_t *>(defer_count), static_cast<const int64_t *>(defer_list),
+                            defer_cap);
 }
 
 cudaError_t prepare_decoupled_kernel() {

@@ -42,7 +42,8 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
                        uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
                        int grid, cudaStream_t st);
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,
-                             int sms, cudaStream_t st);
+                             uint32_t *defer_count, int64_t *defer_list, int defer_cap, int sms, cudaStream_t st);
+constexpr int kDeferCap = 1 << 18;  // deferred blocks of one search (beyond it a lane searches inline)
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, const float *alpha, int64_t H, void *out, int grid,
                     cudaStream_t st);
 cudaError_t launch_encode_e2m1(const float *v, int64_t n, uint8_t *out, int grid, cudaStream_t st);

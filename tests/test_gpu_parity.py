@@ -148,3 +148,29 @@ def test_cjso_alpha_on_an_fp32_midpoint(extra, expect):
         oc, os_, oa = oracle.quantize(w, oracle.CJSO, iters)
         assert ga == oa
         assert np.array_equal(gc, oc) and np.array_equal(gs, os_)
+
+
+def test_decoupled_deferred_blocks_beyond_the_list():
+    """On exactly representable tensors the decoupled search's crossings land
+    exactly on integer k, so nearly every block goes to the plain search:
+    524,288 blocks are more than the list of deferred blocks holds (2^18), so
+    some are searched by the second kernel and the rest inline by the first.
+    Every block compared on a seeded sample (both kinds), and the first rows
+    in full."""
+    rng = np.random.default_rng(44)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rows, cols = 2048, 4096
+    nb = rows * cols // 16
+    e4 = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    d = rng.integers(0x30, 0x70, nb)
+    d[0] = 0x7E
+    mags = rng.integers(0, 8, (nb, 16))
+    mags[:, 5] = 7
+    w = grid[mags] * np.where(rng.integers(0, 2, (nb, 16)) == 1, -1.0, 1.0) * e4[d][:, None] * 2.0 ** -12
+    bits = synthetic.to_bf16_bits(w.reshape(rows, cols).astype(np.float32))
+    gc, gs, ga = gpu_quantize(bits, oracle.CJSO_DECOUPLED, 0)
+    blocks = np.unique(np.concatenate([np.arange(0, 2048), rng.choice(nb, 20000, replace=False)])).astype(np.int64)
+    oc, os_, oa = oracle.quantize_sampled(bits, oracle.CJSO_DECOUPLED, 0, blocks, threads=8)
+    assert ga == oa
+    bad = block_mismatch(gc.reshape(-1, 8)[blocks], gs.reshape(-1)[blocks], oc, os_)
+    assert not bad.any(), bad.sum()
