@@ -229,14 +229,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
 
   uint32_t *my_slot = slot + tid;
   uint32_t *my_mask = mask + tid;
+  uint32_t dn = b < B ? scales[b] : 0u;  // Delta^d0 of the block, fetched one iteration ahead
   // warp-uniform trip count: wf is the warp's first block of the iteration
   for (int64_t wf = warp_first; wf < B; wf += stride, b += stride) {
     const bool live = b < B;
     const int64_t nb = b + stride;
     const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
+    const uint32_t d0 = live ? dn : 0u;
+    dn = nb < B ? scales[nb] : 0u;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
-    const uint32_t d0 = live ? scales[b] : 0u;
     const float s50 = s2_tab[d0].x;
     const float r50 = r_tab[d0];
     const float ev0 = ev_tab[d0];

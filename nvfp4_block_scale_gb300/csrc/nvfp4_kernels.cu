@@ -481,12 +481,18 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   const float r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
   const int U = alpha_unit(alpha);
   build_scale_tables(alpha, s_tab, r_tab);
+  uint32_t sa = 0u, sn = 0u;  // stored scales of the current and the next block, fetched ahead
+  if (!INIT) {
+    sa = ok(b) ? scales[b] : 0u;
+    sn = ok(b + step) ? scales[b + step] : 0u;
+  }
   __syncthreads();
 
   Acc128 num_acc, den_acc;
   for (; ok(b); b += step) {
     const int64_t b2 = b + 2 * step;
     const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
+    const uint32_t sm = (!INIT && ok(b2)) ? scales[b2] : 0u;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
     uint32_t d, d_old = 0xFFu;
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     if (INIT) {
       d = max_rule_code(am, six_a, r6);
     } else {
-      d = d_old = scales[b];
+      d = d_old = sa;
       block_sums(blk, s_tab[d], r_tab[d], P, R);
       if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
     }
@@ -512,6 +518,8 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     a1 = n1;
     n0 = m0;
     n1 = m1;
+    sa = sn;
+    sn = sm;
   }
   u128 num = num_acc.get(), den = den_acc.get();
   block_sum2_u128(num, den, redu);
