@@ -114,7 +114,7 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
  *           not overlap each other or any W.
  *   count   >= 0 (0: nothing is enqueued).  Longer lists are processed in
  *           consecutive slices of NVFP4_GROUP_MAX tensors.  A list holding at
- *           least 4 x L2 bytes of bf16 is cut into parts of about 3 x L2
+ *           least 4 x L2 bytes of bf16 is cut into parts of about 6 x L2
  *           that alternate between `stream` and a second stream owned by the
  *           library (forked from `stream` and joined back into it by events,
  *           so the call can be captured in a CUDA graph), letting one part's

@@ -35,7 +35,7 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 // grouped max rule / FourOverSix: groups of at least kPipeMinL2 x L2 bytes of
 // bf16 run in parts of about kPipePartL2 x L2 on two streams
 constexpr int kPipeMinL2 = 4;
-constexpr int kPipePartL2 = 3;
+constexpr int kPipePartL2 = 6;
 
 struct DevInfo {
   bool ready = false;
