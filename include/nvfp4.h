@@ -114,11 +114,12 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
  *           not overlap each other or any W.
  *   count   >= 0 (0: nothing is enqueued).  Longer lists are processed in
  *           consecutive slices of NVFP4_GROUP_MAX tensors.  A list holding at
- *           least 4 x L2 bytes of bf16 is cut into parts of about 6 x L2
+ *           least 4 x L2 bytes of bf16 is cut into parts of about 3 x L2
  *           that alternate between `stream` and a second stream owned by the
  *           library (forked from `stream` and joined back into it by events,
  *           so the call can be captured in a CUDA graph), letting one part's
- *           max|W| pass overlap another part's quantize pass.  The library
+ *           max|W| pass run on the same SMs as another part's quantize pass
+ *           (which then leaves room for it on every SM).  The library
  *           keeps a small pool of such second streams per device: a call
  *           takes one that no other call holds and that is not part of an
  *           unfinished stream capture, so concurrent calls from several host
@@ -326,6 +327,31 @@ int nvfp4_ffma_probe(int packed, int64_t rounds, float *sink, int64_t sink_float
  */
 int nvfp4_test_fail_allocations(int count);
 int nvfp4_test_first_wait_tries(int64_t tries);
+
+/*
+ * Checked build.  The library compiled with -DNVFP4_CHECKED
+ * (libnvfp4_gb300_checked.so) makes every hot-path kernel (max|W| passes,
+ * max-rule / FourOverSix quantize, CJSO sweeps, decoupled search and its
+ * deferred-block pass, grouped kernels, dequantize) test the index of its
+ * global-memory and table accesses against the buffer's extent first: an
+ * index outside is not accessed (the output it fed is then unspecified) and
+ * the access's site is recorded, the first failure winning.  It is slower and
+ * meant for tests; its results are otherwise the normal build's.
+ *   nvfp4_checked_build(): 1 in the checked build, 0 in the normal one.
+ *   nvfp4_check_take(site): waits for the current device to be idle, then
+ *     moves the first recorded site into *site (host; 0: no failed check) and
+ *     clears it.  Sites are kernel << 8 | access (0x01xx max|W|, 0x02xx
+ *     quantize, 0x03xx CJSO sweep, 0x04xx search, 0x05xx deferred blocks,
+ *     0x06xx dequantize, 0x07xx grouped, 0x0001 the self-test).  In the normal
+ *     build it sets *site = 0.
+ *   nvfp4_check_selftest(i, n, stream): one checked test of i against
+ *     [0, n) that accesses nothing, so a test can see the mechanism record
+ *     site 0x0001 (a no-op in the normal build).
+ * Each returns an nvfp4_status.
+ */
+int nvfp4_checked_build(void);
+int nvfp4_check_take(uint32_t *site);
+int nvfp4_check_selftest(int64_t i, int64_t n, cudaStream_t stream);
 
 /* Human-readable text for a status code (static storage, never NULL). */
 const char *nvfp4_status_string(int status);

@@ -14,7 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .build import LIB_PATH, build as _build
+from .build import CHECKED_LIB_PATH, LIB_PATH, build as _build
 
 MAX, FOUR_OVER_SIX, CJSO, CJSO_DECOUPLED = 0, 1, 2, 3
 MODES = {"max": MAX, "four_over_six": FOUR_OVER_SIX, "cjso": CJSO, "cjso_decoupled": CJSO_DECOUPLED}
@@ -83,6 +83,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.nvfp4_test_fail_allocations.restype = ci
     L.nvfp4_test_first_wait_tries.argtypes = [i64]
     L.nvfp4_test_first_wait_tries.restype = ci
+    L.nvfp4_checked_build.argtypes = []
+    L.nvfp4_checked_build.restype = ci
+    L.nvfp4_check_take.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.nvfp4_check_take.restype = ci
+    L.nvfp4_check_selftest.argtypes = [i64, i64, vp]
+    L.nvfp4_check_selftest.restype = ci
     L.nvfp4_status_string.argtypes = [ci]
     L.nvfp4_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -91,6 +97,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 def library_path() -> str:
     return LIB_PATH
+
+
+def checked_library_path(build: bool = True) -> str:
+    """The bounds-checked build (-DNVFP4_CHECKED), built first if asked; load
+    it with load(path) before any other call of the process."""
+    return _build(checked=True) if build else CHECKED_LIB_PATH
 
 
 # ---------------------------------------------------------------- C ABI mirror
@@ -151,6 +163,29 @@ def nvfp4_test_fail_allocations(count) -> int:
 def nvfp4_test_first_wait_tries(tries) -> int:
     """Test hook: the first bounded device wait gives up after `tries` polls (< 0: normal)."""
     return load().nvfp4_test_first_wait_tries(int(tries))
+
+
+def nvfp4_checked_build() -> int:
+    return load().nvfp4_checked_build()
+
+
+def nvfp4_check_take(site) -> int:
+    """`site`: a ctypes.c_uint32 (byref'd here)."""
+    return load().nvfp4_check_take(ctypes.byref(site))
+
+
+def nvfp4_check_selftest(i, n, stream) -> int:
+    return load().nvfp4_check_selftest(int(i), int(n), stream)
+
+
+def check_take() -> int:
+    """The first failed check's site recorded since the last take (0: none);
+    waits for the device to be idle.  Always 0 in the normal build."""
+    site = ctypes.c_uint32(0)
+    st = nvfp4_check_take(site)
+    if st != NVFP4_OK:
+        raise Nvfp4Error(st, "nvfp4_check_take")
+    return int(site.value)
 
 
 def nvfp4_status_string(status: int) -> str:

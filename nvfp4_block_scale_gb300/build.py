@@ -3,7 +3,8 @@
 Each .cu under csrc/ compiles to an object in parallel, then one shared
 library is linked.  Nothing is installed; the library lands in
 nvfp4_block_scale_gb300/_build/ (git-ignored) and is rebuilt when a source or
-header is newer than it.
+header is newer than it.  build(checked=True) makes the bounds-checked variant
+(-DNVFP4_CHECKED, libnvfp4_gb300_checked.so, objects under _build/checked/).
 """
 from __future__ import annotations
 
@@ -19,6 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libnvfp4_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# the checked build (-DNVFP4_CHECKED: bounds-checked kernel accesses, for tests)
+CHECKED_LIB_PATH = os.path.join(BUILD_DIR, "libnvfp4_gb300_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -45,24 +48,28 @@ def _inputs():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles and links the library; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compiles and links the library (with checked=True the -DNVFP4_CHECKED
+    variant, beside it); returns its path."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and up_to_date(lib_path):
+        return lib_path
+    obj_dir = os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     exe = nvcc()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(exe)), "lib64")
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [exe] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [exe] + NVCC_FLAGS + (["-DNVFP4_CHECKED"] if checked else []) + \
+            (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)
     failed = []
@@ -75,14 +82,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     link = [exe] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + \
         ["-Xlinker", "-rpath," + cuda_lib]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -30,12 +30,14 @@ namespace {
 using namespace nvfp4;
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxIters = 64;
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 // grouped max rule / FourOverSix: groups of at least kPipeMinL2 x L2 bytes of
-// bf16 run in parts of about kPipePartL2 x L2 on two streams
+// bf16 run in parts of about kPipePartL2 x L2 on two streams; there each
+// quantize pass runs one CTA per SM fewer than fit, which leaves the registers
+// of kPipeAmaxCtas amax CTAs (the other stream's) on every SM
 constexpr int kPipeMinL2 = 4;
-constexpr int kPipePartL2 = 6;
+constexpr int kPipePartL2 = 3;
+constexpr int kPipeAmaxCtas = 2;
 
 struct DevInfo {
   bool ready = false;
@@ -373,9 +375,11 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
   // over its tiles.  A group of at least kPipeMinL2 x L2 of bf16 is cut into
   // parts of about kPipePartL2 x L2 that alternate between the caller's stream
   // and a second stream, so one part's amax pass (HBM-bound) runs beside
-  // another's quantize pass (ALU-bound); smaller groups keep one part per
-  // kGroupMax tensors, which lets the quantize pass re-read from L2 what the
-  // amax pass read last.
+  // another's quantize pass (issue-bound) on the same SMs: the quantize grid
+  // then holds one CTA per SM fewer than fit (with both modes' register counts
+  // that frees room for two amax CTAs) and the amax grid kPipeAmaxCtas per SM.
+  // Smaller groups keep one part per kGroupMax tensors, which lets the
+  // quantize pass re-read from L2 what the amax pass read last.
   int64_t total = 0;
   for (int i = 0; i < count; ++i) total += tensors[i].rows * tensors[i].cols;
   const bool pipe = total * 2 >= int64_t(kPipeMinL2) * d->l2 && count >= 2;
@@ -422,14 +426,17 @@ int nvfp4_quantize_grouped(const nvfp4_tensor *tensors, int count, int mode, int
     }
     const int64_t tiles = g->tile_begin[g->count];
     const int grid = (int)std::max<int64_t>(1, std::min(full, tiles));
+    const int grid_a = sd ? (int)std::max<int64_t>(1, std::min<int64_t>(int64_t(d->sms) * kPipeAmaxCtas, tiles)) : grid;
+    const int grid_q =
+        sd ? (int)std::max<int64_t>(1, std::min<int64_t>(int64_t(d->sms) * std::max(1, d->occ[kq] - 1), tiles)) : grid;
     uint32_t *amax = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + slot * k);
     {
       TraceScope tr(kTrGroupAmax, ps);
-      e = launch_group_amax(*g, amax, grid, ps);
+      e = launch_group_amax(*g, amax, grid_a, ps);
     }
     if (e == cudaSuccess) {
       TraceScope tr(mode == kModeFourOverSix ? kTrGroupQuantFos : kTrGroupQuantMax, ps);
-      e = launch_group_quant(mode, *g, amax, grid, ps);
+      e = launch_group_quant(mode, *g, amax, grid_q, ps);
     }
   }
   delete g;
@@ -578,6 +585,37 @@ int nvfp4_test_fail_allocations(int count) {
 int nvfp4_test_first_wait_tries(int64_t tries) {
   g_first_wait.store(tries < 0 ? -1L : (long)std::min<int64_t>(tries, int64_t(1) << 30));
   return NVFP4_OK;
+}
+
+int nvfp4_checked_build(void) {
+#ifdef NVFP4_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int nvfp4_check_take(uint32_t *site) {
+  if (!site) return NVFP4_ERR_INVALID_ARG;
+  *site = 0u;
+#ifdef NVFP4_CHECKED
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = check_take_kernels(site);
+  if (e == cudaSuccess) e = check_take_decoupled(site);
+  return map_cuda(e);
+#else
+  return NVFP4_OK;
+#endif
+}
+
+int nvfp4_check_selftest(int64_t i, int64_t n, cudaStream_t stream) {
+  DevInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NVFP4_OK) return st;
+  return map_cuda(launch_check_selftest(i, n, stream));
 }
 
 int nvfp4_profiler_enable(int on) {

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   }
   pdl_launch_dependents();
   pdl_wait();
-  const float alpha = alpha_hist[t];
+  const float alpha = NVFP4_IN(t, kMaxIters + 1, kCkDecHist) ? alpha_hist[t] : 0.0f;
   if (tid < 128) {
     const float s = __fmul_rn(alpha, ev_tab[tid]);
     const float s1 = tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
     const bool live = b < B;
     const int64_t nb = b + stride;
     const uint4 n0 = nb < B ? __ldg(W + 2 * nb) : z, n1 = nb < B ? __ldg(W + 2 * nb + 1) : z;
-    const uint32_t d0 = live ? dn : 0u;
+    const uint32_t d0 = live && NVFP4_IN(dn, 128, kCkDecTab) ? dn : 0u;
     dn = nb < B ? scales[nb] : 0u;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
           amb = amb || (go && fabsf(frac) < kAmbig);
           const int K = max(n + (frac > 0.0f ? 1 : 0), 1);
           go = go && K <= kSlotK;
-          if (go) {
+          if (go && NVFP4_IN(K - 1, kSlotK, kCkDecSlot)) {
             atomicAdd(my_slot + (K - 1) * kDecThreads,
                       (X11 << ((sr.x >> (8 * st)) & 0xFFu)) + ((sr.y >> (8 * st)) & 0xFFu));
             atomicOr(my_mask + (K >> 5) * kDecThreads, 1u << (K & 31));
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
           while (bits) {
             const int k = 32 * w + __ffs(bits) - 1;
             bits &= bits - 1u;
-            my_slot[(k - 1) * kDecThreads] = 0u;
+            if (NVFP4_IN(k - 1, kSlotK, kCkDecSlot)) my_slot[(k - 1) * kDecThreads] = 0u;
           }
         }
         path = 2;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
           while (bits) {
             const int k = 32 * w + __ffs(bits) - 1;
             bits &= bits - 1u;
+            if (!NVFP4_IN(k, kDecK, kCkDecTab)) continue;
             const int ks = max(k - 1, 0);
             const uint32_t ev = k > 0 ? my_slot[ks * kDecThreads] : 0u;
             if (k > 0) my_slot[ks * kDecThreads] = 0u;
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
     __syncwarp();
     if (path == 2 && !deferred) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
     __syncwarp();
-    const int bk = best_i >> 1;
+    const int bk = NVFP4_IN(best_i >> 1, kDecK, kCkDecTab) ? best_i >> 1 : 0;
     const uint32_t lb = lo_tab[d0 * kDecK + bk];
     const uint32_t best_d = path == 0 ? d0 : (lb & 0x7Fu) + ((best_i & 1) ? (lb >> 7) : 0u);
     const float sq = path == 0 ? 0.0f : __fmul_rn(alpha, __fmul_rn(ev0, m_tab[bk]));
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
 // or a block outside the exact-integer range): the plain search, one block
 // per thread.  Launched as a programmatic dependent of k_decoupled; waits for
 // it before reading the list.
-__global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *__restrict__ W,
+__global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *__restrict__ W, int64_t B,
                                                                    const float *__restrict__ alpha_hist, int t,
                                                                    uint8_t *__restrict__ scales,
                                                                    uint32_t *__restrict__ codes32,
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *
   }
   pdl_launch_dependents();
   pdl_wait();
-  const float alpha = alpha_hist[t];
+  const float alpha = NVFP4_IN(t, kMaxIters + 1, kCkDecHist) ? alpha_hist[t] : 0.0f;
   if (tid < 128) {
     const float sv = __fmul_rn(alpha, ev_tab[tid]);
     s2_tab[tid] = make_float2(sv, tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f);
@@ -398,10 +399,12 @@ __global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *
   const int64_t n = min((int64_t)*defer_count, (int64_t)defer_cap);
   for (int64_t i = (int64_t)blockIdx.x * kPlainThreads + tid; i < n; i += (int64_t)gridDim.x * kPlainThreads) {
     const int64_t b = defer_list[i];
+    if (!NVFP4_IN(b, B, kCkPlainList)) continue;
     const uint32_t d0 = scales[b];
+    if (!NVFP4_IN(d0, 128, kCkPlainTab)) continue;
     const float ev0 = ev_tab[d0];
     const int best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
-    const int bk = best_i >> 1;
+    const int bk = NVFP4_IN(best_i >> 1, kDecK, kCkPlainTab) ? best_i >> 1 : 0;
     const uint32_t lb = lo_tab[d0 * kDecK + bk];
     const uint32_t best_d = (lb & 0x7Fu) + ((best_i & 1) ? (lb >> 7) : 0u);
     const float sq = __fmul_rn(alpha, __fmul_rn(ev0, m_tab[bk]));
@@ -439,9 +442,18 @@ cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, 
   cfg.gridDim = dim3((unsigned)sms);
   cfg.blockDim = dim3(kPlainThreads);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, k_decoupled_plain, w, static_cast<const float *>(alpha_hist), t, scales, c,
+  return cudaLaunchKernelEx(&cfg, k_decoupled_plain, w, B, static_cast<const float *>(alpha_hist), t, scales, c,
                             static_cast<const uint32_t *>(defer_count), static_cast<const int64_t *>(defer_list),
                             defer_cap);
+}
+
+cudaError_t check_take_decoupled(uint32_t *site) {
+#ifdef NVFP4_CHECKED
+  return check_take_here(site);
+#else
+  (void)site;
+  return cudaSuccess;
+#endif
 }
 
 cudaError_t prepare_decoupled_kernel() {

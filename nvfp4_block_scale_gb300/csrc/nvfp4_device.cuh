@@ -13,6 +13,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -343,5 +344,59 @@ __device__ __forceinline__ float cand_err_m2p(float s, float m2P, float R) {
 // are no-ops when the launch carries no programmatic dependency.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Checked build (-DNVFP4_CHECKED).  The hot-path kernels test the index of
+// each global-memory and table access against its buffer's extent before
+// making it: NVFP4_IN(i, n, site) is true for 0 <= i < n; otherwise the access
+// is skipped and `site` is recorded (the first failure wins) in a device word
+// of the translation unit, which nvfp4_check_take reads and clears.  Without
+// the define NVFP4_IN is the constant true and its arguments are not
+// evaluated, so the normal build is unchanged.
+// ---------------------------------------------------------------------------
+
+// Sites: kernel << 8 | access.
+enum : unsigned {
+  kCkSelfTest = 0x0001u,
+  kCkAmaxW = 0x0101u, kCkAmaxPart = 0x0102u,
+  kCkBulkChunk = 0x0111u, kCkBulkStage = 0x0112u, kCkBulkPart = 0x0113u,
+  kCkFoldPart = 0x0121u,
+  kCkQuantW = 0x0201u, kCkQuantTab = 0x0202u, kCkQuantCodes = 0x0203u, kCkQuantScales = 0x0204u,
+  kCkSweepW = 0x0301u, kCkSweepScales = 0x0302u, kCkSweepTab = 0x0303u, kCkSweepCodes = 0x0304u,
+  kCkSweepPartIn = 0x0305u, kCkSweepPartOut = 0x0306u, kCkSweepHist = 0x0307u,
+  kCkDecW = 0x0401u, kCkDecScales = 0x0402u, kCkDecTab = 0x0403u, kCkDecSlot = 0x0404u, kCkDecList = 0x0405u,
+  kCkDecCodes = 0x0406u, kCkDecHist = 0x0407u,
+  kCkPlainList = 0x0501u, kCkPlainW = 0x0502u, kCkPlainScales = 0x0503u, kCkPlainTab = 0x0504u,
+  kCkPlainCodes = 0x0505u,
+  kCkDequantIn = 0x0601u, kCkDequantTab = 0x0602u, kCkDequantOut = 0x0603u,
+  kCkGroupTensor = 0x0701u, kCkGroupW = 0x0702u, kCkGroupAmax = 0x0703u, kCkGroupTab = 0x0704u,
+  kCkGroupOut = 0x0705u,
+};
+
+#ifdef NVFP4_CHECKED
+static __device__ unsigned int g_check_site;  // this translation unit's first failed check (0: none)
+
+__device__ __forceinline__ bool ck_in(int64_t i, int64_t n, unsigned site) {
+  const bool in = i >= 0 && i < n;
+  if (!in) atomicCAS(&g_check_site, 0u, site);
+  return in;
+}
+#define NVFP4_IN(i, n, site) ::nvfp4::ck_in((int64_t)(i), (int64_t)(n), (site))
+
+// Reads and clears this translation unit's word (the device must be idle);
+// a nonzero value goes to *site unless *site already holds one.
+static inline cudaError_t check_take_here(uint32_t *site) {
+  uint32_t v = 0u;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_check_site, sizeof v);
+  if (e == cudaSuccess && v != 0u) {
+    const uint32_t z = 0u;
+    e = cudaMemcpyToSymbol(g_check_site, &z, sizeof z);
+    if (*site == 0u) *site = v;
+  }
+  return e;
+}
+#else
+#define NVFP4_IN(i, n, site) true
+#endif
 
 }  // namespace nvfp4

@@ -8,6 +8,7 @@
 namespace nvfp4 {
 
 enum { kModeMax = 0, kModeFourOverSix = 1, kModeCjso = 2, kModeCjsoDecoupled = 3 };
+constexpr int kMaxIters = 64;  // CJSO iterations per call at most (the alpha history holds kMaxIters + 1)
 enum { kKernAmax = 0, kKernQuantMax, kKernQuantFos, kKernCjso, kKernDequant, kKernGroupAmax,
        kKernGroupQuantMax, kKernGroupQuantFos, kKernAmaxLdg, kKernCount };
 
@@ -68,6 +69,11 @@ cudaError_t prepare_gemm_tc_kernels();
 cudaError_t prepare_decoupled_kernel();
 cudaError_t prepare_quant_kernels();
 int max_active_ctas(int which);
+// checked build (NVFP4_CHECKED): per translation unit, read and clear the
+// first failed check's site into *site (if *site is 0); no-ops otherwise
+cudaError_t check_take_kernels(uint32_t *site);
+cudaError_t check_take_decoupled(uint32_t *site);
+cudaError_t launch_check_selftest(int64_t i, int64_t n, cudaStream_t st);
 int64_t ffma_probe_fmas_per_thread(int packed, int64_t rounds);
 cudaError_t launch_ffma_probe(int packed, int64_t rounds, int grid, float *sink, cudaStream_t st);
 int ffma_probe_threads();

@@ -129,7 +129,7 @@ __device__ __forceinline__ void alpha_terms(uint32_t M, float P, float R, int U,
 __device__ __forceinline__ float fold_alpha(const uint32_t *__restrict__ part, int n, uint32_t *red) {
   uint32_t m = 0;
   for (int i = threadIdx.x; i < n; i += 4 * kThreads) {  // four loads in flight per thread
-    const uint32_t a = part[i];
+    const uint32_t a = NVFP4_IN(i, n, kCkFoldPart) ? part[i] : 0u;
     const uint32_t b = i + kThreads < n ? part[i + kThreads] : 0u;
     const uint32_t c = i + 2 * kThreads < n ? part[i + 2 * kThreads] : 0u;
     const uint32_t d = i + 3 * kThreads < n ? part[i + 3 * kThreads] : 0u;
@@ -183,10 +183,13 @@ __global__ void __launch_bounds__(kThreads) k_amax_partials(const uint4 *__restr
     if (base + (int64_t)(kAmaxUnroll - 1) * kThreads < n16) {
       // whole tile: every load issued before the first use (volatile keeps the order)
 #pragma unroll
-      for (int u = 0; u < kAmaxUnroll; ++u)
-        asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
-                     : "l"(W + base + (int64_t)u * kThreads));
+      for (int u = 0; u < kAmaxUnroll; ++u) {
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (NVFP4_IN(base + (int64_t)u * kThreads, n16, kCkAmaxW))
+          asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                       : "l"(W + base + (int64_t)u * kThreads));
+      }
     } else {
 #pragma unroll
       for (int u = 0; u < kAmaxUnroll; ++u) {
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_bulk(const uint4 *__restrict_
   auto bytes_of = [&](int64_t ch) { return (uint32_t)(min(kUnits, n16 - ch * kUnits) * 16); };
   auto issue = [&](int64_t ch, int st) {
     const uint32_t mb = smem_addr(&mbar[st]), nb = bytes_of(ch);
+    if (!NVFP4_IN(ch * kUnits + nb / 16 - 1, n16, kCkBulkChunk) || !NVFP4_IN(st, kAmaxStages, kCkBulkStage)) return;
     asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(mb), "r"(nb) : "memory");
     asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_addr(stage + (int64_t)st * kUnits)), "l"(src + ch * kAmaxChunk), "r"(nb), "r"(mb)
@@ -275,7 +279,8 @@ __global__ void __launch_bounds__(kThreads) k_amax_bulk(const uint4 *__restrict_
     const uint4 *p = stage + (int64_t)st * kUnits;
     const int units = (int)(bytes_of(ch) / 16);
     for (int i = threadIdx.x; i < units; i += kThreads) {
-      const uint4 v = p[i];
+      const uint4 v = NVFP4_IN((int64_t)st * kUnits + i, (int64_t)kAmaxStages * kUnits, kCkBulkStage)
+                          ? p[i] : make_uint4(0u, 0u, 0u, 0u);
       asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.x));
       asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.y));
       asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.z));
@@ -336,9 +341,11 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
   }
   auto ok = [&](int64_t x) { return ranged ? x < end : x > end; };
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  uint4 a0 = ok(b) ? __ldg(W + 2 * b) : z, a1 = ok(b) ? __ldg(W + 2 * b + 1) : z;
+  const bool v0 = ok(b) && NVFP4_IN(2 * b + 1, 2 * B, kCkQuantW);
+  uint4 a0 = v0 ? __ldg(W + 2 * b) : z, a1 = v0 ? __ldg(W + 2 * b + 1) : z;
   const int64_t b1 = b + step;
-  uint4 n0 = ok(b1) ? __ldg(W + 2 * b1) : z, n1 = ok(b1) ? __ldg(W + 2 * b1 + 1) : z;
+  const bool v1 = ok(b1) && NVFP4_IN(2 * b1 + 1, 2 * B, kCkQuantW);
+  uint4 n0 = v1 ? __ldg(W + 2 * b1) : z, n1 = v1 ? __ldg(W + 2 * b1 + 1) : z;
   if (threadIdx.x < 128) {  // alpha-independent part of the tables
     const float ev = e4m3_value(threadIdx.x);
     ev_tab[threadIdx.x] = ev;
@@ -360,16 +367,19 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
 
   for (; ok(b); b += step) {
     const int64_t b2 = b + 2 * step;
-    const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
+    const bool v2 = ok(b2) && NVFP4_IN(2 * b2 + 1, 2 * B, kCkQuantW);
+    const uint4 m0 = v2 ? __ldg(W + 2 * b2) : z, m1 = v2 ? __ldg(W + 2 * b2 + 1) : z;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
-    const uint32_t d6 = max_rule_code(am, six_a, r6);
+    uint32_t d6 = max_rule_code(am, six_a, r6);
+    if (!NVFP4_IN(d6, 128, kCkQuantTab)) d6 = 0u;
     uint32_t c0, c1, d = d6;
     float P6, R6;
     quant16<FOS>(blk, s_tab[d6], r_tab[d6], c0, c1, P6, R6);
     if (FOS) {
       // [FOS-02] keep scale_m4 iff its dequant error is strictly lower.
-      const uint32_t d4 = c4_tab[d6];
+      uint32_t d4 = c4_tab[d6];
+      if (!NVFP4_IN(d4, 128, kCkQuantTab)) d4 = 0u;
       uint32_t e0, e1;
       float P4, R4;
       quant16<true>(blk, s_tab[d4], r_tab[d4], e0, e1, P4, R4);
@@ -378,9 +388,11 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
       c0 = use4 ? e0 : c0;
       c1 = use4 ? e1 : c1;
     }
-    codes32[2 * b] = c0;  // two 4-byte stores: codes is only 4-byte aligned
-    codes32[2 * b + 1] = c1;
-    scales[b] = (uint8_t)d;
+    if (NVFP4_IN(2 * b + 1, 2 * B, kCkQuantCodes)) {
+      codes32[2 * b] = c0;  // two 4-byte stores: codes is only 4-byte aligned
+      codes32[2 * b + 1] = c1;
+    }
+    if (NVFP4_IN(b, B, kCkQuantScales)) scales[b] = (uint8_t)d;
     a0 = n0;
     a1 = n1;
     n0 = m0;
@@ -392,16 +404,6 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
 // a5: CJSO sweeps
 // ---------------------------------------------------------------------------
 
-// One sweep over all blocks, one block per thread.  INIT: max rule from the
-// amax partials.  Otherwise: alpha from the previous sweep's partial sums
-// ([SOAR-A]), sums with the stored Delta, Delta* ([SOAR-D]) rounded to E4M3,
-// re-quantize ([SOAR-SCHED]).  Every sweep stores Delta, writes its CTA's
-// partial sums sum Delta*P and sum Delta^2*R, and records alpha in
-// alpha_hist[t].  Sweeps chain by programmatic dependent launch: each prefetches
-// its first blocks of W (an input, final before the chain began) and then
-// waits for the previous sweep before reading the partials and the scales.
-// `descending` alternates between sweeps so that each starts on the part of
-// W the previous one read last (still in L2 when W is larger than L2).
 // One sweep over all blocks, one block per thread.  INIT: max rule from the
 // amax partials.  Otherwise: alpha from the previous sweep's partial sums
 // ([SOAR-A]), sums with the stored Delta, Delta* ([SOAR-D]) rounded to E4M3,
@@ -439,8 +441,10 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   int64_t b = descending ? B - 1 - i0 : i0;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   auto ok = [&](int64_t x) { return x >= 0 && x < B; };
-  uint4 a0 = ok(b) ? __ldg(W + 2 * b) : z, a1 = ok(b) ? __ldg(W + 2 * b + 1) : z;
-  uint4 n0 = ok(b + step) ? __ldg(W + 2 * (b + step)) : z, n1 = ok(b + step) ? __ldg(W + 2 * (b + step) + 1) : z;
+  const bool v0 = ok(b) && NVFP4_IN(2 * b + 1, 2 * B, kCkSweepW);
+  const bool v1 = ok(b + step) && NVFP4_IN(2 * (b + step) + 1, 2 * B, kCkSweepW);
+  uint4 a0 = v0 ? __ldg(W + 2 * b) : z, a1 = v0 ? __ldg(W + 2 * b + 1) : z;
+  uint4 n0 = v1 ? __ldg(W + 2 * (b + step)) : z, n1 = v1 ? __ldg(W + 2 * (b + step) + 1) : z;
   if (threadIdx.x < 128) {
     const float ev = e4m3_value(threadIdx.x);
     ev_tab[threadIdx.x] = ev;
@@ -461,7 +465,8 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     }
     block_sum2_u128(num, den, redu);
     if (threadIdx.x == 0) {
-      const float prev = alpha_hist[t - 1];  // the alpha the partial sums were formed with
+      // the alpha the partial sums were formed with
+      const float prev = NVFP4_IN(t - 1, kMaxIters + 1, kCkSweepHist) ? alpha_hist[t - 1] : 0.0f;
       if (den == 0) {
         sh_alpha = prev;
       } else {
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     alpha = sh_alpha;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    alpha_hist[t] = alpha;
+    if (NVFP4_IN(t, kMaxIters + 1, kCkSweepHist)) alpha_hist[t] = alpha;
     if (write_alpha) *alpha_out = alpha;
   }
   const float six_a = __fmul_rn(alpha, 6.0f);
@@ -483,16 +488,17 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   build_scale_tables(alpha, s_tab, r_tab);
   uint32_t sa = 0u, sn = 0u;  // stored scales of the current and the next block, fetched ahead
   if (!INIT) {
-    sa = ok(b) ? scales[b] : 0u;
-    sn = ok(b + step) ? scales[b + step] : 0u;
+    sa = ok(b) && NVFP4_IN(b, B, kCkSweepScales) ? scales[b] : 0u;
+    sn = ok(b + step) && NVFP4_IN(b + step, B, kCkSweepScales) ? scales[b + step] : 0u;
   }
   __syncthreads();
 
   Acc128 num_acc, den_acc;
   for (; ok(b); b += step) {
     const int64_t b2 = b + 2 * step;
-    const uint4 m0 = ok(b2) ? __ldg(W + 2 * b2) : z, m1 = ok(b2) ? __ldg(W + 2 * b2 + 1) : z;
-    const uint32_t sm = (!INIT && ok(b2)) ? scales[b2] : 0u;
+    const bool v2 = ok(b2) && NVFP4_IN(2 * b2 + 1, 2 * B, kCkSweepW);
+    const uint4 m0 = v2 ? __ldg(W + 2 * b2) : z, m1 = v2 ? __ldg(W + 2 * b2 + 1) : z;
+    const uint32_t sm = (!INIT && ok(b2) && NVFP4_IN(b2, B, kCkSweepScales)) ? scales[b2] : 0u;
     Block16 blk;
     const uint32_t am = unpack16(a0, a1, blk);
     uint32_t d, d_old = 0xFFu;
@@ -500,19 +506,22 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     if (INIT) {
       d = max_rule_code(am, six_a, r6);
     } else {
-      d = d_old = sa;
+      d = d_old = NVFP4_IN(sa, 128, kCkSweepTab) ? sa : 0u;
       block_sums(blk, s_tab[d], r_tab[d], P, R);
       if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
     }
+    if (!NVFP4_IN(d, 128, kCkSweepTab)) d = 0u;
     if (write_codes) {
       uint32_t c0, c1;
       quant16<true>(blk, s_tab[d], r_tab[d], c0, c1, P, R);
-      codes32[2 * b] = c0;
-      codes32[2 * b + 1] = c1;
+      if (NVFP4_IN(2 * b + 1, 2 * B, kCkSweepCodes)) {
+        codes32[2 * b] = c0;
+        codes32[2 * b + 1] = c1;
+      }
     } else if (d != d_old) {  // an unchanged Delta re-quantizes to the same codes, P and R
       block_sums(blk, s_tab[d], r_tab[d], P, R);
     }
-    scales[b] = (uint8_t)d;
+    if (NVFP4_IN(b, B, kCkSweepScales)) scales[b] = (uint8_t)d;
     alpha_terms(m_tab[d], P, R, U, num_acc, den_acc);
     a0 = n0;
     a1 = n1;
@@ -566,6 +575,7 @@ __global__ void __launch_bounds__(kThreads) k_group_amax(const __grid_constant__
   uint32_t m = 0u;
   while (tile < end) {
     while (tile >= g.tile_begin[t + 1]) ++t;  // (t + 1 <= count: tile < tile_begin[count])
+    if (!NVFP4_IN(t, g.count, kCkGroupTensor)) break;  // (uniform over the CTA)
     const int64_t stop = min(end, g.tile_begin[t + 1]);
     const int64_t nt = min((int64_t)kGroupAmaxTiles, stop - tile);
     const uint4 *W = static_cast<const uint4 *>(g.t[t].W);
@@ -605,8 +615,9 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
   int64_t tile = T * (blockIdx.x + 1) / gridDim.x - 1;  // walks down to lo
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   auto load = [&](int64_t tl, int tt, uint4 &x0, uint4 &x1) {
-    const int64_t b = (tl - g.tile_begin[tt]) * kGroupTile + threadIdx.x;
-    if (b < g.t[tt].B) {
+    const bool known = NVFP4_IN(tt, g.count, kCkGroupTensor);
+    const int64_t b = (tl - g.tile_begin[known ? tt : 0]) * kGroupTile + threadIdx.x;
+    if (known && b < g.t[tt].B) {
       const uint4 *W = static_cast<const uint4 *>(g.t[tt].W);
       x0 = __ldg(W + 2 * b);
       x1 = __ldg(W + 2 * b + 1);
@@ -621,7 +632,7 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
     t = tn = group_find(g, tile);
     load(tile, t, a0, a1);
     if (tile - 1 >= lo) {
-      while (tile - 1 < g.tile_begin[tn]) --tn;
+      while (NVFP4_IN(tn, g.count, kCkGroupTensor) && tile - 1 < g.tile_begin[tn]) --tn;
       load(tile - 1, tn, n0, n1);
     }
   }
@@ -639,10 +650,11 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
   int cur = -1;  // tensor whose tables are loaded
   float alpha = 0.0f, six_a = 0.0f, r6 = 0.0f;
   for (; tile >= lo; --tile) {
+    if (!NVFP4_IN(t, g.count, kCkGroupTensor)) break;  // (uniform over the CTA)
     int tm = tn;
     uint4 m0 = z, m1 = z;
     if (tile - 2 >= lo) {
-      while (tile - 2 < g.tile_begin[tm]) --tm;
+      while (NVFP4_IN(tm, g.count, kCkGroupTensor) && tile - 2 < g.tile_begin[tm]) --tm;
       load(tile - 2, tm, m0, m1);
     }
     if (t != cur) {  // uniform over the CTA
@@ -664,12 +676,14 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
     if (b < gt.B) {
       Block16 blk;
       const uint32_t am = unpack16(a0, a1, blk);
-      const uint32_t d6 = max_rule_code(am, six_a, r6);
+      uint32_t d6 = max_rule_code(am, six_a, r6);
+      if (!NVFP4_IN(d6, 128, kCkGroupTab)) d6 = 0u;
       uint32_t c0, c1, d = d6;
       float P6, R6;
       quant16<FOS>(blk, s_tab[d6], r_tab[d6], c0, c1, P6, R6);
       if (FOS) {  // [FOS-02] keep scale_m4 iff its dequant error is strictly lower
-        const uint32_t d4 = c4_tab[d6];
+        uint32_t d4 = c4_tab[d6];
+        if (!NVFP4_IN(d4, 128, kCkGroupTab)) d4 = 0u;
         uint32_t e0, e1;
         float P4, R4;
         quant16<true>(blk, s_tab[d4], r_tab[d4], e0, e1, P4, R4);
@@ -706,7 +720,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint32_t *__restrict
   __syncthreads();
   for (int64_t h = (int64_t)blockIdx.x * kThreads + threadIdx.x; h < H; h += (int64_t)gridDim.x * kThreads) {
     const uint32_t cw = __ldg(codes32 + h);
-    const float s = s_tab[__ldg(scales + (h >> 1))];
+    const float s = NVFP4_IN(h >> 1, H / 2, kCkDequantIn) ? s_tab[__ldg(scales + (h >> 1))] : 0.0f;
     uint32_t o[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -797,6 +811,26 @@ cudaLaunchConfig_t make_cfg(int grid, cudaStream_t st) {
   return cfg;
 }
 }  // namespace
+
+// Checked build: a kernel that makes one checked test of i against [0, n)
+// and accesses nothing (the check mechanism's own test).
+__global__ void k_check_selftest(int64_t i, int64_t n) {
+  if (NVFP4_IN(i, n, kCkSelfTest)) asm volatile("");
+}
+
+cudaError_t launch_check_selftest(int64_t i, int64_t n, cudaStream_t st) {
+  k_check_selftest<<<1, 1, 0, st>>>(i, n);
+  return cudaGetLastError();
+}
+
+cudaError_t check_take_kernels(uint32_t *site) {
+#ifdef NVFP4_CHECKED
+  return check_take_here(site);
+#else
+  (void)site;
+  return cudaSuccess;
+#endif
+}
 
 cudaError_t launch_amax_partials(const void *W, int64_t n16, uint32_t *part, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);

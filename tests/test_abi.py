@@ -150,3 +150,15 @@ def test_gemm_rejects_bad_arguments():
     assert nv.nvfp4_gemm(A16, A16, A16, 4, 16, A16, 257, A16, None) == INVALID
     assert nv.nvfp4_gemm(A16 + 4, A16, A16, 4, 16, A16, 1, A16, None) == MISALIGNED
     assert nv.nvfp4_gemm(A16, A16, A16, 4, 16, A16 + 8, 1, A16, None) == MISALIGNED
+
+
+def test_checked_build_exports_the_same_functions():
+    """The bounds-checked variant exports every declared function and says
+    which build it is (no device needed); take rejects a null pointer."""
+    lib = ctypes.CDLL(nv.checked_library_path(build=True))
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.nvfp4_checked_build() == 1
+    assert nv.load().nvfp4_checked_build() == 0
+    lib.nvfp4_check_take.argtypes = [ctypes.c_void_p]
+    assert lib.nvfp4_check_take(None) == INVALID
