@@ -311,13 +311,13 @@ int nvfp4_quantize(const void *W, int64_t rows, int64_t cols, int mode, int iter
     const bool plain = mode == kModeCjso;
     {
       TraceScope tr(kTrCjsoInit, stream);
-      e = launch_cjso_sweep(true, W, H, amax_part, g_amax, nullptr, 0, part[0], hist, 0, scales, codes,
+      e = launch_cjso_sweep(true, T > 0, W, H, amax_part, g_amax, nullptr, 0, part[0], hist, 0, scales, codes,
                             plain && T == 0, alpha, T == 0, g_cjso, stream);
     }
     for (int t = 1; t <= T && e == cudaSuccess; ++t) {
       TraceScope tr(kTrCjsoIter, stream);
-      e = launch_cjso_sweep(false, W, H, amax_part, g_amax, part[(t - 1) & 1], g_cjso, part[t & 1], hist, t,
-                            scales, codes, plain && t == T, alpha, t == T, g_cjso, stream);
+      e = launch_cjso_sweep(false, t < T, W, H, amax_part, g_amax, part[(t - 1) & 1], g_cjso, part[t & 1], hist,
+                            t, scales, codes, plain && t == T, alpha, t == T, g_cjso, stream);
     }
     if (e == cudaSuccess && !plain) {
       TraceScope tr(kTrDecoupled, stream);

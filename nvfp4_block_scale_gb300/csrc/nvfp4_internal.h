@@ -38,10 +38,11 @@ int amax_bulk_chunks(int64_t n16);
 cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
                                  uint8_t *codes, uint8_t *scales, float *alpha, int grid, int ranged,
                                  cudaStream_t st);
-cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
-                       const ulonglong2 *part_in, int n_in, ulonglong2 *part_out, float *alpha_hist, int t,
-                       uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
-                       int grid, cudaStream_t st);
+// sums: form and write the partial sums of the next alpha step (false for the last sweep of a call)
+cudaError_t launch_cjso_sweep(bool init, bool sums, const void *W, int64_t H, const uint32_t *amax_part,
+                              int n_amax, const ulonglong2 *part_in, int n_in, ulonglong2 *part_out,
+                              float *alpha_hist, int t, uint8_t *scales, uint8_t *codes, int write_codes,
+                              float *alpha_out, int write_alpha, int grid, cudaStream_t st);
 cudaError_t launch_decoupled(const void *W, int64_t B, const float *alpha_hist, int t, uint8_t *scales, uint8_t *codes,
                              uint32_t *defer_count, int64_t *defer_list, int defer_cap, int sms, cudaStream_t st);
 constexpr int kDeferCap = 1 << 18;  // deferred blocks of one search (beyond it a lane searches inline)

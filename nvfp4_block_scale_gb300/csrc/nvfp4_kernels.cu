@@ -417,10 +417,11 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
 // W (an input, final before the chain began) and then waits for the previous
 // sweep before reading the partials and the scales.  `descending` alternates
 // between sweeps so that each starts on the part of W the previous one read
-// last (still in L2 when W is larger than L2).
+// last (still in L2 when W is larger than L2).  A sweep without SUMS (the last
+// of a call: no alpha step follows) neither forms nor writes the partial sums.
 __device__ __forceinline__ int alpha_unit(float alpha) { return (int)((__float_as_uint(alpha) >> 23) & 0xFFu) - 127 - 48; }
 
-template <bool INIT>
+template <bool INIT, bool SUMS>
 __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict__ W, int64_t B,
                                                          const uint32_t *__restrict__ amax_part, int n_amax,
                                                          const ulonglong2 *__restrict__ part_in, int n_in,
@@ -513,16 +514,16 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     if (!NVFP4_IN(d, 128, kCkSweepTab)) d = 0u;
     if (write_codes) {
       uint32_t c0, c1;
-      quant16<true>(blk, s_tab[d], r_tab[d], c0, c1, P, R);
+      quant16<SUMS>(blk, s_tab[d], r_tab[d], c0, c1, P, R);
       if (NVFP4_IN(2 * b + 1, 2 * B, kCkSweepCodes)) {
         codes32[2 * b] = c0;
         codes32[2 * b + 1] = c1;
       }
-    } else if (d != d_old) {  // an unchanged Delta re-quantizes to the same codes, P and R
+    } else if (SUMS && d != d_old) {  // an unchanged Delta re-quantizes to the same codes, P and R
       block_sums(blk, s_tab[d], r_tab[d], P, R);
     }
     if (NVFP4_IN(b, B, kCkSweepScales)) scales[b] = (uint8_t)d;
-    alpha_terms(m_tab[d], P, R, U, num_acc, den_acc);
+    if (SUMS) alpha_terms(m_tab[d], P, R, U, num_acc, den_acc);
     a0 = n0;
     a1 = n1;
     n0 = m0;
@@ -530,11 +531,13 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     sa = sn;
     sn = sm;
   }
-  u128 num = num_acc.get(), den = den_acc.get();
-  block_sum2_u128(num, den, redu);
-  if (threadIdx.x == 0) {
-    part_out[2 * blockIdx.x] = make_ulonglong2((unsigned long long)num, (unsigned long long)(num >> 64));
-    part_out[2 * blockIdx.x + 1] = make_ulonglong2((unsigned long long)den, (unsigned long long)(den >> 64));
+  if (SUMS) {
+    u128 num = num_acc.get(), den = den_acc.get();
+    block_sum2_u128(num, den, redu);
+    if (threadIdx.x == 0) {
+      part_out[2 * blockIdx.x] = make_ulonglong2((unsigned long long)num, (unsigned long long)(num >> 64));
+      part_out[2 * blockIdx.x + 1] = make_ulonglong2((unsigned long long)den, (unsigned long long)(den >> 64));
+    }
   }
 }
 
@@ -874,10 +877,10 @@ cudaError_t launch_quant_max_fos(int mode, const void *W, int64_t H, const uint3
   return cudaLaunchKernelEx(&cfg, k_quant_max_fos<kModeMax>, w, B, amax_part, n_amax, c, scales, alpha, ranged);
 }
 
-cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_t *amax_part, int n_amax,
-                              const ulonglong2 *part_in, int n_in, ulonglong2 *part_out, float *alpha_hist, int t,
-                              uint8_t *scales, uint8_t *codes, int write_codes, float *alpha_out, int write_alpha,
-                              int grid, cudaStream_t st) {
+cudaError_t launch_cjso_sweep(bool init, bool sums, const void *W, int64_t H, const uint32_t *amax_part,
+                              int n_amax, const ulonglong2 *part_in, int n_in, ulonglong2 *part_out,
+                              float *alpha_hist, int t, uint8_t *scales, uint8_t *codes, int write_codes,
+                              float *alpha_out, int write_alpha, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = make_cfg(grid, st);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -888,11 +891,10 @@ cudaError_t launch_cjso_sweep(bool init, const void *W, int64_t H, const uint32_
   uint32_t *c = reinterpret_cast<uint32_t *>(codes);
   const int64_t B = H / 2;
   const int descending = (t & 1) == 0;  // amax reads ascending; sweeps alternate from there
-  if (init)
-    return cudaLaunchKernelEx(&cfg, k_cjso_sweep<true>, w, B, amax_part, n_amax, part_in, n_in, part_out,
-                              alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha, descending);
-  return cudaLaunchKernelEx(&cfg, k_cjso_sweep<false>, w, B, amax_part, n_amax, part_in, n_in, part_out,
-                            alpha_hist, t, scales, c, write_codes, alpha_out, write_alpha, descending);
+  auto kern = init ? (sums ? k_cjso_sweep<true, true> : k_cjso_sweep<true, false>)
+                   : (sums ? k_cjso_sweep<false, true> : k_cjso_sweep<false, false>);
+  return cudaLaunchKernelEx(&cfg, kern, w, B, amax_part, n_amax, part_in, n_in, part_out, alpha_hist, t, scales, c,
+                            write_codes, alpha_out, write_alpha, descending);
 }
 
 cudaError_t launch_group_amax(const GroupArgs &g, uint32_t *amax, int grid, cudaStream_t st) {
@@ -953,7 +955,7 @@ int max_active_ctas(int which) {
     case kKernAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_bulk, kThreads, kAmaxBulkSmem); break;
     case kKernQuantMax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeMax>, kThreads, 0); break;
     case kKernQuantFos: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant_max_fos<kModeFourOverSix>, kThreads, 0); break;
-    case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false>, kThreads, 0); break;
+    case kKernCjso: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_cjso_sweep<false, true>, kThreads, 0); break;
     case kKernAmaxLdg: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_amax_partials, kThreads, 0); break;
     case kKernGroupAmax: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_group_amax, kThreads, 0); break;
     case kKernGroupQuantMax:
