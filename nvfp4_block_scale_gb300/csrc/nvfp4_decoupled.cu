@@ -73,12 +73,13 @@ constexpr float kAmbig = 0x1p-13f;
 constexpr size_t kOffMask = (size_t)kSlotK * kDecThreads * 4;
 constexpr size_t kOffLohi = kOffMask + (size_t)4 * kDecThreads * 4;
 constexpr size_t kOffS2 = kOffLohi + 128 * 4 * 4;
-constexpr size_t kOffR = kOffS2 + 128 * 8;
+constexpr size_t kOffR = kOffS2 + 256 * 8;
 constexpr size_t kOffEv = kOffR + 128 * 4;
 constexpr size_t kOffM = kOffEv + 128 * 4;
 constexpr size_t kOffH = kOffM + 104 * 4;
 constexpr size_t kOffStep = kOffH + 8 * 16;
-constexpr size_t kOffLo = kOffStep + 8 * 8;
+constexpr size_t kOffQ = kOffStep + 8 * 32;
+constexpr size_t kOffLo = kOffQ + 8 * 8;
 constexpr size_t kDecSmem = kOffLo + 128 * kDecK;
 static_assert(kDecSmem <= 232448, "dynamic shared memory of one CTA");
 
@@ -99,6 +100,13 @@ __device__ __forceinline__ uint32_t lut8(uint32_t lo4, uint32_t hi4, uint32_t id
 // 2q and 4q^2 of a magnitude code: {0,1,2,3,4,6,8,12}, {0,1,4,9,16,36,64,144}
 __device__ __forceinline__ uint32_t two_q(uint32_t c) { return lut8(0x03020100u, 0x0C080604u, c); }
 __device__ __forceinline__ uint32_t four_q2(uint32_t c) { return lut8(0x09040100u, 0x90402410u, c); }
+
+// Dequant scales of a bracket byte's two candidates: (fl(alpha * lo),
+// fl(alpha * hi)), hi = lo + 1 when bit 7 is set, else lo.
+__device__ __forceinline__ float2 scale_pair(uint32_t lb, float alpha, const float *ev_tab) {
+  const uint32_t lo = lb & 0x7Fu, hi = (lb >> 7) && lo < 0x7Eu ? lo + 1u : lo;
+  return make_float2(__fmul_rn(alpha, ev_tab[lo]), __fmul_rn(alpha, ev_tab[hi]));
+}
 
 // E4M3 codes bracketing dq >= 0: lo = largest with value <= dq, hi = smallest
 // with value >= dq (448 above 448), packed as lo | (hi != lo) << 7.
@@ -161,12 +169,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   uint32_t *slot = reinterpret_cast<uint32_t *>(dsm);            // [k - 1][thread]
   uint32_t *mask = reinterpret_cast<uint32_t *>(dsm + kOffMask);  // [word][thread]
   uint32_t *lohi = reinterpret_cast<uint32_t *>(dsm + kOffLohi);  // [Delta^d0 code][word]
-  float2 *s2_tab = reinterpret_cast<float2 *>(dsm + kOffS2);      // fl(alpha * value) of codes c, c + 1
+  float2 *s2_tab = reinterpret_cast<float2 *>(dsm + kOffS2);      // [bracket byte]: fl(alpha * value) of lo, hi
   float *r_tab = reinterpret_cast<float *>(dsm + kOffR);          // IEEE reciprocal of fl(alpha * value)
   float *ev_tab = reinterpret_cast<float *>(dsm + kOffEv);        // E4M3 values
   float *m_tab = reinterpret_cast<float *>(dsm + kOffM);          // m_k
   float4 *h_rows = reinterpret_cast<float4 *>(dsm + kOffH);       // [code c]: fl(100/b) of c-1 .. c-4
-  uint2 *step_rows = reinterpret_cast<uint2 *>(dsm + kOffStep);   // [code c]: shifts, R4 steps (bytes)
+  uint4 *step_rows = reinterpret_cast<uint4 *>(dsm + kOffStep);   // [code c][0 | 1]: 2^(11 + shift) | R4 step
+  uint2 *q_rows = reinterpret_cast<uint2 *>(dsm + kOffQ);          // [code c]: 2q, 4q^2
   uint8_t *lo_tab = dsm + kOffLo;                                 // [Delta^d0 code][k] bracket byte
   const int tid = threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * kDecThreads;
@@ -182,16 +191,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   if (tid < kDecK) m_tab[tid] = __double2float_rn(__ddiv_rn((double)(50 + tid), 100.0));  // m_k
   if (tid < 8) {  // crossing constants of magnitude code c = tid, steps st = 0..3 -> decision point c-1-st
     float hv[4];
-    uint32_t sh = 0u, r4 = 0u;
+    uint32_t mul[4], r4[4];  // a crossing's slot value is X * mul + r4
 #pragma unroll
     for (int st = 0; st < 4; ++st) {
       const int i = tid - 1 - st;
       hv[st] = i >= 0 ? kHundredOverB[i] : 0.0f;
-      sh |= (uint32_t)(i >= 0 ? kStepShift[i] : 0) << (8 * st);
-      r4 |= (uint32_t)(i >= 0 ? kStepR4[i] : 0) << (8 * st);
+      mul[st] = i >= 0 ? 1u << (11 + kStepShift[i]) : 0u;
+      r4[st] = i >= 0 ? kStepR4[i] : 0u;
     }
     h_rows[tid] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-    step_rows[tid] = make_uint2(sh, r4);
+    step_rows[2 * tid] = make_uint4(mul[0], mul[1], mul[2], mul[3]);
+    step_rows[2 * tid + 1] = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+    q_rows[tid] = make_uint2(two_q(tid), four_q2(tid));
   }
   __syncthreads();
   for (int e = tid; e < 128 * kDecK; e += kDecThreads) {
@@ -219,10 +230,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
   pdl_launch_dependents();
   pdl_wait();
   const float alpha = NVFP4_IN(t, kMaxIters + 1, kCkDecHist) ? alpha_hist[t] : 0.0f;
+  if (tid < 256) s2_tab[tid] = scale_pair(tid, alpha, ev_tab);
   if (tid < 128) {
     const float s = __fmul_rn(alpha, ev_tab[tid]);
-    const float s1 = tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f;
-    s2_tab[tid] = make_float2(s, s1);
     r_tab[tid] = s > 0.0f ? __frcp_rn(s) : 0.0f;
   }
   __syncthreads();
@@ -260,30 +270,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
       for (int j = 0; j < 16; ++j) {
         const float xa = fabsf(elem(blk, j));
         const uint32_t c = (qw[j >> 3] >> (4 * (j & 7))) & 7u;
-        const uint32_t X = __float2uint_rz(__fmul_rn(xa, sc));
-        P += (int)(X * two_q(c));
-        R4 += (int)four_q2(c);
+        // X = xa 2^E (< 2^15) read off the bits of 2^23 + xa 2^E; exact whenever c > 0,
+        // the only case where X is used (a code-0 element adds 0 and has no crossing)
+        const uint32_t X = __float_as_uint(__fmaf_rn(xa, sc, 8388608.0f)) - 0x4B000000u;
+        const uint2 q = q_rows[c];  // 2q, 4q^2
+        P += (int)(X * q.x);
+        R4 += (int)q.y;
         const float v = __fmul_rn(xa, r50);
         const float4 hr = h_rows[c];
-        const uint2 sr = step_rows[c];
+        const uint4 mr = step_rows[2 * c], rr = step_rows[2 * c + 1];
         const float hv[4] = {hr.x, hr.y, hr.z, hr.w};
-        const uint32_t X11 = X << 11;
+        const uint32_t mv[4] = {mr.x, mr.y, mr.z, mr.w}, rv[4] = {rr.x, rr.y, rr.z, rr.w};
         bool go = true;
 #pragma unroll
         for (int st = 0; st < 4; ++st) {  // the element's crossings, in k order: decision points c-1, c-2, ...
           go = go && (int)c > st;
           const float kap = __fmaf_rn(v, hv[st], -50.0f);
-          // kap rounded to the nearest integer n (|kap| < 2^22), and K = ceil(kap)
-          const float tt = __fadd_rn(kap, 12582912.0f);
-          const int n = __float_as_int(tt) - 0x4B400000;
-          const float frac = __fsub_rn(kap, __fsub_rn(tt, 12582912.0f));
-          // within kAmbig of an integer the crossing may be at n or n + 1
-          amb = amb || (go && fabsf(frac) < kAmbig);
-          const int K = max(n + (frac > 0.0f ? 1 : 0), 1);
+          // K = ceil(kap) from an addition rounded up onto the integers of
+          // [2^23, 2^24) (|kap| < 2^22); at least 1, the crossing lies past k = 0
+          const int K = max(__float_as_int(__fadd_ru(kap, 12582912.0f)) - 0x4B400000, 1);
+          // within kAmbig of an integer (its nearest, by the same addition
+          // rounded to nearest) the crossing may be at either neighbour
+          const float rn = __fsub_rn(__fadd_rn(kap, 12582912.0f), 12582912.0f);
+          amb = amb || (go && fabsf(__fsub_rn(kap, rn)) < kAmbig);
           go = go && K <= kSlotK;
           if (go && NVFP4_IN(K - 1, kSlotK, kCkDecSlot)) {
-            atomicAdd(my_slot + (K - 1) * kDecThreads,
-                      (X11 << ((sr.x >> (8 * st)) & 0xFFu)) + ((sr.y >> (8 * st)) & 0xFFu));
+            atomicAdd(my_slot + (K - 1) * kDecThreads, X * mv[st] + rv[st]);
             atomicOr(my_mask + (K >> 5) * kDecThreads, 1u << (K & 31));
           }
         }
@@ -301,31 +313,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
         }
         path = 2;
       } else {
-        // scan the breakpoints in k order
-        float best_g = __int_as_float(0x7F800000);
+        // scan the breakpoints in k order.  P and R4 are held as the bits of
+        // the floats 2^23 + P and 2^23 + R4 (both < 2^23, so adding 0x4B000000
+        // to the integer is exact); the scaling subtracts the 2^23 back.
         const float c23 = __fmul_rn(-8388608.0f, nsc);
         const uint32_t *lm = lohi + d0 * 4;
         const uint8_t *lrow = lo_tab + d0 * kDecK;
+        int Pb = P + 0x4B000000, Rb = R4 + 0x4B000000;
+        // k = 0 (always a breakpoint: the start state)
+        float best_g;
+        {
+          const float m2P = __fmaf_rn(__int_as_float(Pb), nsc, c23);
+          const float R = __fmaf_rn(__int_as_float(Rb), 0.25f, -2097152.0f);
+          const float2 sp = s2_tab[lrow[0]];
+          const float glo = cand_err_m2p(sp.x, m2P, R);
+          const float ghi = cand_err_m2p(sp.y, m2P, R);
+          best_g = glo;
+          best_i = ghi < glo ? 1 : 0;
+          best_g = ghi < glo ? ghi : glo;
+        }
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          uint32_t bits = lm[w] | my_mask[w * kDecThreads];
+          uint32_t bits = (lm[w] | my_mask[w * kDecThreads]) & (w == 0 ? ~1u : ~0u);
           my_mask[w * kDecThreads] = 0u;
           while (bits) {
             const int k = 32 * w + __ffs(bits) - 1;
             bits &= bits - 1u;
             if (!NVFP4_IN(k, kDecK, kCkDecTab)) continue;
-            const int ks = max(k - 1, 0);
-            const uint32_t ev = k > 0 ? my_slot[ks * kDecThreads] : 0u;
-            if (k > 0) my_slot[ks * kDecThreads] = 0u;
-            P -= (int)(ev >> 11);
-            R4 -= (int)(ev & 0x7FFu);
-            // exact int -> float: (2^23 + v) - 2^23, folded into the scaling
-            const float m2P = __fmaf_rn(__uint_as_float((uint32_t)P | 0x4B000000u), nsc, c23);
-            const float R = __fmaf_rn(__uint_as_float((uint32_t)R4 | 0x4B000000u), 0.25f, -2097152.0f);
-            const uint32_t lb = lrow[k];
-            const float2 sp = s2_tab[lb & 0x7Fu];
+            const uint32_t ev = my_slot[(k - 1) * kDecThreads];
+            my_slot[(k - 1) * kDecThreads] = 0u;
+            Pb -= (int)(ev >> 11);
+            Rb -= (int)(ev & 0x7FFu);
+            const float m2P = __fmaf_rn(__int_as_float(Pb), nsc, c23);
+            const float R = __fmaf_rn(__int_as_float(Rb), 0.25f, -2097152.0f);
+            const float2 sp = s2_tab[lrow[k]];
             const float glo = cand_err_m2p(sp.x, m2P, R);
-            const float ghi = cand_err_m2p((lb >> 7) ? sp.y : sp.x, m2P, R);
+            const float ghi = cand_err_m2p(sp.y, m2P, R);
             const bool tlo = glo < best_g;
             best_g = tlo ? glo : best_g;
             best_i = tlo ? 2 * k : best_i;
@@ -347,7 +370,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decoupled(const uint4 *__res
       }
     }
     __syncwarp();
-    if (path == 2 && !deferred) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab, m_tab, lo_tab);
+    if (path == 2 && !deferred) best_i = search_plain(W, b, alpha, ev0, d0, s2_tab + 128, m_tab, lo_tab);
     __syncwarp();
     const int bk = NVFP4_IN(best_i >> 1, kDecK, kCkDecTab) ? best_i >> 1 : 0;
     const uint32_t lb = lo_tab[d0 * kDecK + bk];
@@ -378,7 +401,7 @@ __global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *
                                                                    const int64_t *__restrict__ defer_list,
                                                                    int defer_cap) {
   __shared__ float ev_tab[128], m_tab[kDecK];
-  __shared__ float2 s2_tab[128];
+  __shared__ float2 s2_tab[128];  // [code c]: fl(alpha * value) of c, c + 1
   __shared__ uint8_t lo_tab[128 * kDecK];
   const int tid = threadIdx.x;
   if (tid < 128) ev_tab[tid] = e4m3_value(tid);
@@ -391,10 +414,7 @@ __global__ void __launch_bounds__(kPlainThreads) k_decoupled_plain(const uint4 *
   pdl_launch_dependents();
   pdl_wait();
   const float alpha = NVFP4_IN(t, kMaxIters + 1, kCkDecHist) ? alpha_hist[t] : 0.0f;
-  if (tid < 128) {
-    const float sv = __fmul_rn(alpha, ev_tab[tid]);
-    s2_tab[tid] = make_float2(sv, tid < 127 ? __fmul_rn(alpha, ev_tab[tid + 1]) : 0.0f);
-  }
+  if (tid < 128) s2_tab[tid] = scale_pair(tid | 0x80u, alpha, ev_tab);
   __syncthreads();
   const int64_t n = min((int64_t)*defer_count, (int64_t)defer_cap);
   for (int64_t i = (int64_t)blockIdx.x * kPlainThreads + tid; i < n; i += (int64_t)gridDim.x * kPlainThreads) {
