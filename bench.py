@@ -251,24 +251,38 @@ def input_sha256(w_bits: np.ndarray) -> str:
     return hashlib.sha256(np.ascontiguousarray(w_bits).tobytes()).hexdigest()
 
 
-def oracle_rows(mode: str, cols: int, rows: int) -> int:
+def oracle_rows(mode: str, cols: int, rows: int, batch: int = 1) -> int:
     """Rows of the bounded CPU sample per mode (a few seconds of oracle work on
     16 host cores): the decoupled search is ~100x slower per element."""
     budget = {"max": 1 << 23, "four_over_six": 1 << 23, "cjso": 1 << 22, "cjso_decoupled": 1 << 18,
-              "dequant": 1 << 23}[mode]
+              "dequant": 1 << 23, "swizzle": 1 << 23, "gemv": (1 << 23) // batch, "gemm": (1 << 23) // batch}[mode]
     return int(max(16, min(rows, budget // cols)))
 
 
-def oracle_time_mode(w_bits, mode: str, iters: int, min_seconds: float):
+# the oracle function a mode is timed against: the allocation-free entry point computes the
+# max rule / FourOverSix; the consumers read a max-rule tensor
+ORACLE_OF = {"max_noalloc": "max", "four_over_six_noalloc": "four_over_six"}
+
+
+def oracle_time_mode(w_bits, mode: str, iters: int, min_seconds: float, batch: int = 1):
     """The oracle as it stands, on all host cores, on the first rows of W;
-    returns (GB/s of bf16, seconds, repetitions, rows)."""
+    returns (GB/s of bf16 W, seconds, repetitions, rows)."""
     import oracle
+    import synthetic
     threads = os.cpu_count() or 1
-    rows = oracle_rows(mode, w_bits.shape[1], w_bits.shape[0])
+    mode = ORACLE_OF.get(mode, mode)
+    rows = oracle_rows(mode, w_bits.shape[1], w_bits.shape[0], batch)
     sample = np.ascontiguousarray(w_bits[:rows])
-    if mode == "dequant":
+    cols = sample.shape[1]
+    if mode in CONSUMERS:
         c, s, a = oracle.quantize(sample, oracle.MAX, 0, threads=threads)
-        fn = lambda: oracle.dequantize(c, s, a, rows, sample.shape[1])
+        if mode == "dequant":
+            fn = lambda: oracle.dequantize(c, s, a, rows, cols)
+        elif mode == "swizzle":
+            fn = lambda: oracle.swizzle_scales(s, rows, cols // 16)
+        else:  # the W4A16 product with `batch` vectors
+            x = synthetic.gaussian(batch, cols, 1.0, 7)
+            fn = lambda: oracle.gemv(c, s, a, rows, cols, x)
     else:
         fn = lambda: oracle.quantize(sample, MODE_IDS[mode], iters, threads=threads)
     t0 = time.perf_counter()
@@ -282,15 +296,21 @@ def oracle_time_mode(w_bits, mode: str, iters: int, min_seconds: float):
     return reps * sample.nbytes / el / 1e9, el, reps, rows
 
 
-def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=4.0):
+def oracle_cpu_baseline(w_bits, modes, iters, min_seconds=4.0, batch=1):
     """Per mode and for the whole step: the oracle on host cores, bounded samples."""
     threads = os.cpu_count() or 1
     per, tot_bytes, tot_s = {}, 0.0, 0.0
     for m in modes:
-        gbs, el, reps, rows = oracle_time_mode(w_bits, m, iters, min_seconds)
+        gbs, el, reps, rows = oracle_time_mode(w_bits, m, iters, min_seconds, batch)
+        what = {"dequant": " (dequantize of the max-rule output)",
+                "swizzle": " (scale layout of the max-rule output)",
+                "gemv": f" (oracle_gemv of the max-rule output, {batch} vector(s))",
+                "gemm": f" (oracle_gemv of the max-rule output, {batch} vector(s))"}.get(m, "")
+        if m in ORACLE_OF:
+            what = f" (the {ORACLE_OF[m]} oracle: the function this entry point computes)"
         per[m] = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                   "sample": f"rows 0..{rows - 1} of {w_bits.shape[0]}x{w_bits.shape[1]}, {reps} repetition(s) "
-                            f"in {el:.1f} s" + (" (dequantize of the max-rule output)" if m == "dequant" else "")}
+                            f"in {el:.1f} s" + what}
         tot_bytes += w_bits.shape[1] * 2  # one row of bf16 per mode: combine per-row costs
         tot_s += w_bits.shape[1] * 2 / (gbs * 1e9)
     step = {"value": tot_bytes / tot_s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -661,7 +681,7 @@ def run_ours(args, modes):
                   "steps": k_e2e, "pipelining": "2 buffer slots; H2D, kernels and D2H on three streams"}
 
     if rank == 0 and ws == 1:
-        step_cpu, per_cpu = oracle_cpu_baseline(w_bits, [m for m in modes if m in HOT_PATH], args.iters)
+        step_cpu, per_cpu = oracle_cpu_baseline(w_bits, list(modes), args.iters, batch=args.batch)
         out["cpu_baseline"] = step_cpu
         for m, v in per_cpu.items():
             per_mode[m]["cpu_baseline"] = v
@@ -749,6 +769,16 @@ def run_model(args, modes, fp32=None, steps=None):
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
+    # kernels per step, counted by the library's tracer (a grouped call's launches depend on
+    # how the library cuts the group into parts; the search's deferred-block kernel is traced
+    # with the search)
+    nv.nvfp4_profiler_reset()
+    nv.nvfp4_profiler_enable(1)
+    step()
+    torch.cuda.synchronize()
+    nv.nvfp4_profiler_enable(0)
+    traced = nv.profiler_report()
+    launches = sum(c for c, _ in traced.values()) + traced.get("k_decoupled", (0, 0.0))[0]
     gstep = graph_of(step)
     clocks = ClockSampler(local)
     for attempt in range(2):
@@ -761,10 +791,6 @@ def run_model(args, modes, fp32=None, steps=None):
         csum["remeasured"] = True
     del gstep
     value = len(mids) * 2 * n * steps / (ms / 1e3) / 1e9
-    launches = 0
-    for m in mids:
-        launches += 2 * math.ceil(len(Ws) / nv.NVFP4_GROUP_MAX) if m in (0, 1) else \
-            len(Ws) * kernels_per_call(m, args.iters)
     out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": steps,
            "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16 in, fp32 arithmetic, e2m1+e4m3 out", "data": "synthetic",
