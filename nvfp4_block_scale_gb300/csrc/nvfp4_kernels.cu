@@ -365,12 +365,17 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
   }
   __syncthreads();
 
-  for (; ok(b); b += step) {
-    const int64_t b2 = b + 2 * step;
-    const bool v2 = ok(b2) && NVFP4_IN(2 * b2 + 1, 2 * B, kCkQuantW);
-    const uint4 m0 = v2 ? __ldg(W + 2 * b2) : z, m1 = v2 ? __ldg(W + 2 * b2 + 1) : z;
+  // The walk, unrolled three times: each step issues the loads of the block two steps
+  // ahead into the buffer it has just consumed, so the three buffers take turns
+  // without register copies.
+  auto fetch = [&](int64_t x, uint4 &y0, uint4 &y1) {
+    const bool v = ok(x) && NVFP4_IN(2 * x + 1, 2 * B, kCkQuantW);
+    y0 = v ? __ldg(W + 2 * x) : z;
+    y1 = v ? __ldg(W + 2 * x + 1) : z;
+  };
+  auto quantize_block = [&](const uint4 &x0, const uint4 &x1) {
     Block16 blk;
-    const uint32_t am = unpack16(a0, a1, blk);
+    const uint32_t am = unpack16(x0, x1, blk);
     uint32_t d6 = max_rule_code(am, six_a, r6);
     if (!NVFP4_IN(d6, 128, kCkQuantTab)) d6 = 0u;
     uint32_t c0, c1, d = d6;
@@ -393,10 +398,20 @@ __global__ void __launch_bounds__(kThreads) k_quant_max_fos(const uint4 *__restr
       codes32[2 * b + 1] = c1;
     }
     if (NVFP4_IN(b, B, kCkQuantScales)) scales[b] = (uint8_t)d;
-    a0 = n0;
-    a1 = n1;
-    n0 = m0;
-    n1 = m1;
+  };
+  uint4 m0, m1;
+  while (ok(b)) {
+    fetch(b + 2 * step, m0, m1);
+    quantize_block(a0, a1);
+    b += step;
+    if (!ok(b)) break;
+    fetch(b + 2 * step, a0, a1);
+    quantize_block(n0, n1);
+    b += step;
+    if (!ok(b)) break;
+    fetch(b + 2 * step, n0, n1);
+    quantize_block(m0, m1);
+    b += step;
   }
 }
 
@@ -495,19 +510,23 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
   __syncthreads();
 
   Acc128 num_acc, den_acc;
-  for (; ok(b); b += step) {
-    const int64_t b2 = b + 2 * step;
-    const bool v2 = ok(b2) && NVFP4_IN(2 * b2 + 1, 2 * B, kCkSweepW);
-    const uint4 m0 = v2 ? __ldg(W + 2 * b2) : z, m1 = v2 ? __ldg(W + 2 * b2 + 1) : z;
-    const uint32_t sm = (!INIT && ok(b2) && NVFP4_IN(b2, B, kCkSweepScales)) ? scales[b2] : 0u;
+  // The walk, unrolled three times as in k_quant_max_fos: each step issues the loads of the
+  // block two steps ahead (W and its stored scale) into the buffer it has just consumed.
+  auto fetch = [&](int64_t x, uint4 &y0, uint4 &y1, uint32_t &ys) {
+    const bool v = ok(x) && NVFP4_IN(2 * x + 1, 2 * B, kCkSweepW);
+    y0 = v ? __ldg(W + 2 * x) : z;
+    y1 = v ? __ldg(W + 2 * x + 1) : z;
+    ys = (!INIT && ok(x) && NVFP4_IN(x, B, kCkSweepScales)) ? scales[x] : 0u;
+  };
+  auto sweep_block = [&](const uint4 &x0, const uint4 &x1, uint32_t xs) {
     Block16 blk;
-    const uint32_t am = unpack16(a0, a1, blk);
+    const uint32_t am = unpack16(x0, x1, blk);
     uint32_t d, d_old = 0xFFu;
     float P, R;
     if (INIT) {
       d = max_rule_code(am, six_a, r6);
     } else {
-      d = d_old = NVFP4_IN(sa, 128, kCkSweepTab) ? sa : 0u;
+      d = d_old = NVFP4_IN(xs, 128, kCkSweepTab) ? xs : 0u;
       block_sums(blk, s_tab[d], r_tab[d], P, R);
       if (R > 0.0f) d = e4m3_code(__fdiv_rn(P, __fmul_rn(alpha, R)));
     }
@@ -524,12 +543,21 @@ __global__ void __launch_bounds__(kThreads) k_cjso_sweep(const uint4 *__restrict
     }
     if (NVFP4_IN(b, B, kCkSweepScales)) scales[b] = (uint8_t)d;
     if (SUMS) alpha_terms(m_tab[d], P, R, U, num_acc, den_acc);
-    a0 = n0;
-    a1 = n1;
-    n0 = m0;
-    n1 = m1;
-    sa = sn;
-    sn = sm;
+  };
+  uint4 m0, m1;
+  uint32_t sm;
+  while (ok(b)) {
+    fetch(b + 2 * step, m0, m1, sm);
+    sweep_block(a0, a1, sa);
+    b += step;
+    if (!ok(b)) break;
+    fetch(b + 2 * step, a0, a1, sa);
+    sweep_block(n0, n1, sn);
+    b += step;
+    if (!ok(b)) break;
+    fetch(b + 2 * step, n0, n1, sn);
+    sweep_block(m0, m1, sm);
+    b += step;
   }
   if (SUMS) {
     u128 num = num_acc.get(), den = den_acc.get();
@@ -652,16 +680,21 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
 
   int cur = -1;  // tensor whose tables are loaded
   float alpha = 0.0f, six_a = 0.0f, r6 = 0.0f;
-  for (; tile >= lo; --tile) {
-    if (!NVFP4_IN(t, g.count, kCkGroupTensor)) break;  // (uniform over the CTA)
-    int tm = tn;
-    uint4 m0 = z, m1 = z;
-    if (tile - 2 >= lo) {
-      while (NVFP4_IN(tm, g.count, kCkGroupTensor) && tile - 2 < g.tile_begin[tm]) --tm;
-      load(tile - 2, tm, m0, m1);
+  // The walk, unrolled three times as in k_quant_max_fos: each step looks up the tensor of
+  // the tile two steps ahead (searching down from its neighbour's) and issues its loads into
+  // the buffer it has just consumed.
+  auto fetch = [&](int64_t tl, int from, int &tt, uint4 &y0, uint4 &y1) {
+    tt = from;
+    y0 = z;
+    y1 = z;
+    if (tl >= lo) {
+      while (NVFP4_IN(tt, g.count, kCkGroupTensor) && tl < g.tile_begin[tt]) --tt;
+      load(tl, tt, y0, y1);
     }
-    if (t != cur) {  // uniform over the CTA
-      alpha = __fdiv_rn(__uint_as_float(amax[t] << 16), 2688.0f);  // [SOAR-Q] alpha = max|W| / (6*448)
+  };
+  auto quant_tile = [&](const uint4 &x0, const uint4 &x1, int tt) {
+    if (tt != cur) {  // uniform over the CTA
+      alpha = __fdiv_rn(__uint_as_float(amax[tt] << 16), 2688.0f);  // [SOAR-Q] alpha = max|W| / (6*448)
       six_a = __fmul_rn(alpha, 6.0f);
       r6 = six_a > 0.0f ? __frcp_rn(six_a) : 0.0f;
       __syncthreads();  // the previous tensor's tables are no longer read
@@ -671,14 +704,14 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
         r_tab[threadIdx.x] = sv > 0.0f ? __frcp_rn(sv) : 0.0f;
       }
       __syncthreads();
-      cur = t;
+      cur = tt;
     }
-    const GroupTensor &gt = g.t[t];
-    if (threadIdx.x == 0 && tile == g.tile_begin[t]) *gt.alpha = alpha;
-    const int64_t b = (tile - g.tile_begin[t]) * kGroupTile + threadIdx.x;
+    const GroupTensor &gt = g.t[tt];
+    if (threadIdx.x == 0 && tile == g.tile_begin[tt]) *gt.alpha = alpha;
+    const int64_t b = (tile - g.tile_begin[tt]) * kGroupTile + threadIdx.x;
     if (b < gt.B) {
       Block16 blk;
-      const uint32_t am = unpack16(a0, a1, blk);
+      const uint32_t am = unpack16(x0, x1, blk);
       uint32_t d6 = max_rule_code(am, six_a, r6);
       if (!NVFP4_IN(d6, 128, kCkGroupTab)) d6 = 0u;
       uint32_t c0, c1, d = d6;
@@ -700,12 +733,20 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
       codes32[2 * b + 1] = c1;
       gt.scales[b] = (uint8_t)d;
     }
-    a0 = n0;
-    a1 = n1;
-    n0 = m0;
-    n1 = m1;
-    t = tn;
-    tn = tm;
+  };
+  int tm = 0;
+  uint4 m0, m1;
+  while (tile >= lo) {  // (t, tn, tm: the tensors of the tiles in a0/a1, n0/n1, m0/m1)
+    if (!NVFP4_IN(t, g.count, kCkGroupTensor)) break;  // (uniform over the CTA)
+    fetch(tile - 2, tn, tm, m0, m1);
+    quant_tile(a0, a1, t);
+    if (--tile < lo || !NVFP4_IN(tn, g.count, kCkGroupTensor)) break;
+    fetch(tile - 2, tm, t, a0, a1);
+    quant_tile(n0, n1, tn);
+    if (--tile < lo || !NVFP4_IN(tm, g.count, kCkGroupTensor)) break;
+    fetch(tile - 2, t, tn, n0, n1);
+    quant_tile(m0, m1, tm);
+    --tile;
   }
 }
 
