@@ -123,6 +123,27 @@ def _parallel_normal(rows: int, cols: int, std: float, seed: int, chunk_rows: in
     return a
 
 
+def gaussian_bf16_large(rows: int, cols: int, std: float, seed: int, chunk_rows: int = 256) -> np.ndarray:
+    """N(0, std) as bf16 bits [rows, cols] for tensors too large to hold in
+    float32 as well: chunk c (of `chunk_rows` rows) is drawn from the c-th child
+    of SeedSequence(seed) on host threads and rounded to bf16 in place."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    out = np.empty((rows, cols), np.uint16)
+    nch = (rows + chunk_rows - 1) // chunk_rows
+    seqs = np.random.SeedSequence(seed).spawn(nch)
+
+    def fill(c):
+        lo, hi = c * chunk_rows, min(rows, (c + 1) * chunk_rows)
+        a = np.random.Generator(np.random.PCG64(seqs[c])).standard_normal((hi - lo, cols), dtype=np.float32)
+        a *= np.float32(std)
+        out[lo:hi] = to_bf16_bits(a)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(nch)))
+    return out
+
+
 def mlp_70b(seed: int = 4, rows: int = 8192, cols: int = 28672) -> np.ndarray:
     """N(0, 0.01) with 0.05 % of entries set to +-U(0.3, 1.0).  The Gaussian
     part is drawn in row chunks from child streams of SeedSequence(seed)
