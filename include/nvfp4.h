@@ -332,7 +332,8 @@ int nvfp4_test_first_wait_tries(int64_t tries);
  * Checked build.  The library compiled with -DNVFP4_CHECKED
  * (libnvfp4_gb300_checked.so) makes every hot-path kernel (max|W| passes,
  * max-rule / FourOverSix quantize, CJSO sweeps, decoupled search and its
- * deferred-block pass, grouped kernels, dequantize) test the index of its
+ * deferred-block pass, grouped kernels, dequantize; so every quantize and
+ * dequantize entry point, the allocation-free one included) test the index of its
  * global-memory and table accesses against the buffer's extent first: an
  * index outside is not accessed (the output it fed is then unspecified) and
  * the access's site is recorded, the first failure winning.  It is slower and
