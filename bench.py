@@ -26,9 +26,9 @@ Prints one JSON line (rank 0).
                device time) against its bound.
   e2e          the same step through the C ABI with pinned host buffers: H2D of
                W and D2H of every output inside the timed region.
-  workloads    the 224-tensor Llama-3-8B-shaped stack (FourOverSix grouped,
-               decoupled CJSO(5)) as a second record (skipped with --no-stack
-               or N > 1).
+  workloads    further records of the same form (skipped with --no-stack or
+               N > 1): the 224-tensor Llama-3-8B-shaped stack (FourOverSix
+               grouped, decoupled CJSO(5)) and the 4096x14336 tensor (every mode).
 
 --impl reference runs the C oracle on a bounded sample of the same workload
 per step and prints the same line with "impl": "reference".
@@ -960,7 +960,8 @@ def main():
     ap.add_argument("--layers", type=int, default=32, help=f"layers of the {MODEL} stack (1..32)")
     ap.add_argument("--stack-steps", type=int, default=4, help=f"timed steps of the {MODEL} record")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors of the gemv (1..8) and gemm (1..256) modes")
-    ap.add_argument("--no-stack", action="store_true", help=f"skip the {MODEL} record of the headline run")
+    ap.add_argument("--no-stack", action="store_true",
+                    help=f"skip the further records ({MODEL}, mlp_up) of the headline run")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (eager; no graphs, e2e, oracle or tracing): for profiler runs")
     args = ap.parse_args()
@@ -980,6 +981,9 @@ def main():
                 and args.modes is None):
             out["workloads"] = {MODEL: run_model(args, ("four_over_six", "cjso_decoupled"), out.get("fp32_peak"),
                                                   steps=args.stack_steps)}
+            up = argparse.Namespace(**vars(args))
+            up.workload = "mlp_up"
+            out["workloads"]["mlp_up"] = run_ours(up, WORKLOADS["mlp_up"][2])
     if out is not None:
         print(json.dumps(out), flush=True)
 
