@@ -754,6 +754,8 @@ __global__ void __launch_bounds__(kThreads) k_group_quant(const __grid_constant_
 // a8: dequantize
 // ---------------------------------------------------------------------------
 
+constexpr int kDqUnroll = 2;
+
 __global__ void __launch_bounds__(kThreads) k_dequant(const uint32_t *__restrict__ codes32,
                                                       const uint8_t *__restrict__ scales,
                                                       const float *__restrict__ alpha_p, int64_t H,
@@ -762,17 +764,32 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint32_t *__restrict
   const float alpha = *alpha_p;
   s_tab[threadIdx.x] = __fmul_rn(alpha, e4m3_value(threadIdx.x));  // kThreads == 256
   __syncthreads();
-  for (int64_t h = (int64_t)blockIdx.x * kThreads + threadIdx.x; h < H; h += (int64_t)gridDim.x * kThreads) {
-    const uint32_t cw = __ldg(codes32 + h);
-    const float s = NVFP4_IN(h >> 1, H / 2, kCkDequantIn) ? s_tab[__ldg(scales + (h >> 1))] : 0.0f;
-    uint32_t o[4];
+  // kDqUnroll units per thread per trip, a grid stride apart (each unit's accesses coalesced
+  // across the warp as in a plain grid-stride loop), all loads issued before the first use
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t h0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; h0 < H; h0 += kDqUnroll * stride) {
+    uint32_t cw[kDqUnroll], sc[kDqUnroll];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 q = e2m1x2_to_f32x2((cw >> (8 * k)) & 0xFFu);  // signed codes
-      __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(q.x, s), __fmul_rn(q.y, s));
-      o[k] = *reinterpret_cast<uint32_t *>(&p);
+    for (int u = 0; u < kDqUnroll; ++u) {
+      const int64_t h = h0 + u * stride;
+      const bool in = h < H && NVFP4_IN(h >> 1, H / 2, kCkDequantIn);
+      cw[u] = in ? __ldg(codes32 + h) : 0u;
+      sc[u] = in ? __ldg(scales + (h >> 1)) : 0u;
     }
-    out[h] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int u = 0; u < kDqUnroll; ++u) {
+      const int64_t h = h0 + u * stride;
+      if (h >= H) break;
+      const float s = s_tab[sc[u]];
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 q = e2m1x2_to_f32x2((cw[u] >> (8 * k)) & 0xFFu);  // signed codes
+        __nv_bfloat162 p = __floats2bfloat162_rn(__fmul_rn(q.x, s), __fmul_rn(q.y, s));
+        o[k] = *reinterpret_cast<uint32_t *>(&p);
+      }
+      out[h] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
